@@ -1,0 +1,571 @@
+#!/usr/bin/env python3
+"""Paged KV-cache decode benchmark on one GB300: KV-read GB/s (fraction of the
+measured HBM peak) and attended tokens/s.
+
+A step is one pass of the hot path over one batch: the cache write of the
+step's new K/V (reshape_and_cache through the slot mapping), then paged decode
+attention of every sequence (split-K partitions plus the log-sum-exp merge).
+The headline workload is the LLaMA-2-7B-shaped decode: 64 sequences x 4096
+tokens, 32 q = 32 kv heads, head_dim 128, bf16, 16-token blocks scattered over
+a pool of 1.25x the demand.  Its 4.3 GB of K/V per step exceed the 129 MB L2,
+so consecutive steps read from HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
+replica on its own GPU (the path has no cross-GPU exchange); the time is the
+max over ranks and the value counts the bytes of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode KV-read GB/s (% of GB300 HBM peak) and attended tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--no-also", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+# ---- environment -----------------------------------------------------------------
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "paged_kv_cache_98_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(name: str):
+    """DRAM bytes per launch recorded by an ncu capture of the current kernel
+    sources (profiles/<name>.md, line 'traffic_bytes_per_launch: X src: H'), scaled
+    to a full launch; None when absent or taken on other sources."""
+    path = os.path.join(ROOT, "profiles", name + ".md")
+    try:
+        text = open(path, encoding="utf-8").read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+src:\s*([0-9a-f]+)", text)
+    if not m or m.group(2) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---- one workload on the GPU ---------------------------------------------------------
+class GpuStep:
+    """Device-resident state of one workload and its step (cache write, decode
+    attention, and prefill-chunk attention when the workload has chunks)."""
+
+    def __init__(self, w, dev):
+        import numpy as np
+        import torch
+
+        import paged_kv_cache_98_gb300 as pkv
+        import workloads
+
+        self.w, self.dev, self.pkv = w, dev, pkv
+        k, v, q = workloads.values_device(w, dev)
+        self.ks = self.vs = 1.0
+        if w.kv_dtype == workloads.E4M3:
+            # per-tensor scales amax / 448 of the source tensors
+            self.ks = float(np.float32(k.float().abs().max().item()) / np.float32(448.0))
+            self.vs = float(np.float32(v.float().abs().max().item()) / np.float32(448.0))
+        shape = (w.num_blocks, w.num_kv_heads, 16, w.head_dim)
+        cdt = torch.uint8 if w.kv_dtype == workloads.E4M3 else k.dtype
+        self.kc = torch.zeros(shape, dtype=cdt, device=dev)
+        self.vc = torch.zeros(shape, dtype=cdt, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        chunk = 1 << 16
+        for a in range(0, len(w.fill_rows), chunk):
+            r = torch.from_numpy(w.fill_rows[a:a + chunk]).to(dev)
+            pkv.reshape_and_cache(k.index_select(0, r).contiguous(), v.index_select(0, r).contiguous(),
+                                  self.kc, self.vc, torch.from_numpy(w.fill_slots[a:a + chunk]).to(dev),
+                                  self.ks, self.vs, device_errors=self.err)
+        r = torch.from_numpy(w.new_rows).to(dev)
+        self.k_new = k.index_select(0, r).contiguous()
+        self.v_new = v.index_select(0, r).contiguous()
+        self.slots = torch.from_numpy(w.new_slots).to(dev)
+        qsl = workloads.query_start_loc(w.q_lens)
+        self.dec = w.decode_ids()
+        self.pre = w.prefill_ids()
+        self.q_dec = q.index_select(0, torch.from_numpy(qsl[self.dec].astype(np.int64)).to(dev)).contiguous()
+        self.bt = torch.from_numpy(np.ascontiguousarray(w.block_tables[self.dec])).to(dev)
+        self.cl = torch.from_numpy(np.ascontiguousarray(w.context_lens[self.dec])).to(dev)
+        self.max_ctx = int(w.context_lens[self.dec].max()) if len(self.dec) else 0
+        self.out = torch.empty_like(self.q_dec)
+        S, H, D = self.q_dec.shape
+        self.ws_bytes = pkv.decode_workspace_size(S, H, D, self.max_ctx, 0)
+        self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+        self.parts = max(1, -(-self.max_ctx // 512))
+        if len(self.pre):
+            rows = np.concatenate([np.arange(qsl[s], qsl[s + 1]) for s in self.pre]).astype(np.int64)
+            self.q_pre = q.index_select(0, torch.from_numpy(rows).to(dev)).contiguous()
+            self.bt_pre = torch.from_numpy(np.ascontiguousarray(w.block_tables[self.pre])).to(dev)
+            self.cl_pre = torch.from_numpy(np.ascontiguousarray(w.context_lens[self.pre])).to(dev)
+            self.qsl_pre = torch.from_numpy(workloads.query_start_loc(w.q_lens[self.pre])).to(dev)
+            self.max_q_pre = int(w.q_lens[self.pre].max())
+            self.max_ctx_pre = int(w.context_lens[self.pre].max())
+            self.out_pre = torch.empty_like(self.q_pre)
+            nb = pkv.prefill_workspace_size(self.q_pre.shape[0], H, D, self.max_ctx_pre,
+                                            self.max_q_pre)
+            self.ws_pre = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+        del k, v, q
+        torch.cuda.synchronize(dev)
+        if pkv.check_errors(self.err) != 0:
+            raise RuntimeError("device-side checks failed while filling the cache")
+
+    def launches_per_step(self) -> int:
+        n = 1  # cache write
+        if len(self.dec):
+            n += 1 + (1 if self.parts > 1 else 0)
+        if len(self.pre):
+            n += 1 + (1 if -(-self.max_ctx_pre // 512) > 1 else 0)
+        return n
+
+    def write(self):
+        self.pkv.reshape_and_cache(self.k_new, self.v_new, self.kc, self.vc, self.slots, self.ks,
+                                   self.vs, device_errors=self.err)
+
+    def decode(self):
+        if len(self.dec):
+            self.pkv.paged_attention_decode(
+                self.out, self.q_dec, self.kc, self.vc, self.bt, self.cl, self.w.scale,
+                max_context_len=self.max_ctx, k_scale=self.ks, v_scale=self.vs, workspace=self.ws,
+                device_errors=self.err)
+
+    def prefill(self):
+        if len(self.pre):
+            self.pkv.paged_attention_prefill_chunk(
+                self.out_pre, self.q_pre, self.kc, self.vc, self.bt_pre, self.cl_pre, self.qsl_pre,
+                self.w.scale, max_q_len=self.max_q_pre, max_context_len=self.max_ctx_pre,
+                k_scale=self.ks, v_scale=self.vs, workspace=self.ws_pre, device_errors=self.err)
+
+    def step(self):
+        self.write()
+        self.decode()
+        self.prefill()
+
+    def timed(self, steps: int, warmup: int, barrier=None):
+        """Times `steps` steps; per-step events around the decode and prefill calls."""
+        import torch
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize(self.dev)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        if barrier:
+            barrier()
+        torch.cuda.synchronize(self.dev)
+        t0.record()
+        for e in ev:
+            e[0].record()
+            self.write()
+            e[1].record()
+            self.decode()
+            e[2].record()
+            self.prefill()
+            e[3].record()
+        t1.record()
+        torch.cuda.synchronize(self.dev)
+        if barrier:
+            barrier()
+        total = t0.elapsed_time(t1)
+        dec = [e[1].elapsed_time(e[2]) for e in ev]
+        pre = [e[2].elapsed_time(e[3]) for e in ev]
+        wr = [e[0].elapsed_time(e[1]) for e in ev]
+        return {"total_ms": total, "decode_ms": statistics.mean(dec),
+                "prefill_ms": statistics.mean(pre), "write_ms": statistics.mean(wr),
+                "decode_ms_median": statistics.median(dec)}
+
+    def e2e(self, steps: int, warmup: int):
+        """Same step through the public API from pinned host buffers: the step's
+        inputs are copied in and its output read back inside the timed region."""
+        import torch
+        host = {}
+        for name in ("k_new", "v_new", "slots", "q_dec", "bt", "cl"):
+            t = getattr(self, name)
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            host[name] = h
+        out_h = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+        h2d = sum(h.numel() * h.element_size() for h in host.values())
+        d2h = out_h.numel() * out_h.element_size()
+
+        def one():
+            for name, h in host.items():
+                getattr(self, name).copy_(h, non_blocking=True)
+            self.step()
+            out_h.copy_(self.out, non_blocking=True)
+
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize(self.dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            one()
+        b.record()
+        torch.cuda.synchronize(self.dev)
+        return a.elapsed_time(b) / steps, h2d, d2h
+
+
+def unique_kv_bytes(w) -> int:
+    import numpy as np
+    blocks = set()
+    for s in w.decode_ids():
+        nb = -(-int(w.context_lens[s]) // 16)
+        blocks.update(w.block_tables[s, :nb].tolist())
+    return len(blocks) * 16 * 2 * w.num_kv_heads * w.head_dim * w.kv_elem_bytes
+
+
+def describe(w) -> str:
+    import numpy as np
+    dt = {0: "fp16", 1: "bf16", 2: "fp8-e4m3"}
+    ctx = w.context_lens[w.decode_ids()]
+    return (f"{w.name}: {len(ctx)} decode seqs (ctx {int(ctx.min())}..{int(ctx.max())}, "
+            f"mean {float(np.mean(ctx)):.0f}), {w.num_heads} q / {w.num_kv_heads} kv heads, "
+            f"head_dim {w.head_dim}, block 16, q {dt[w.q_dtype]}, kv {dt[w.kv_dtype]}"
+            + (f", {len(w.prefill_ids())} prefill chunks of {int(w.q_lens[w.prefill_ids()].max())}"
+               if len(w.prefill_ids()) else ""))
+
+
+# ---- CPU oracle ------------------------------------------------------------------------
+class OracleSample:
+    """The oracle's cache write + decode on a sample shaped like the workload
+    (context ctx, H/Hkv heads, head_dim D): `nseq` sequences, `groups` KV heads
+    each.  Set-up (drawing values, filling the host cache) is not timed."""
+
+    def __init__(self, H, Hkv, D, ctx, kv_dtype, nseq, groups):
+        import numpy as np
+
+        import oracle
+        import workloads
+        self.o, self.np = oracle, np
+        g = H // Hkv
+        self.kv_dtype = kv_dtype
+        w = workloads.independent("cpu sample", 77, [ctx] * nseq, g * groups, groups, D,
+                                  workloads.BF16, kv_dtype)
+        self.w = w
+        k, v, q = workloads.values_cpu(w)
+        eb = 1 if kv_dtype == workloads.E4M3 else 2
+        self.kc = np.zeros(w.num_blocks * groups * 16 * D * eb, np.uint8)
+        self.vc = np.zeros_like(self.kc)
+        self.sc = 0.01 if kv_dtype == workloads.E4M3 else 1.0
+        oracle.reshape_and_cache(np.ascontiguousarray(k[w.fill_rows]),
+                                 np.ascontiguousarray(v[w.fill_rows]), self.kc, self.vc,
+                                 w.fill_slots, w.num_blocks, 16, workloads.BF16, kv_dtype,
+                                 self.sc, self.sc)
+        self.k_new = np.ascontiguousarray(k[w.new_rows])
+        self.v_new = np.ascontiguousarray(v[w.new_rows])
+        self.q = np.ascontiguousarray(q)
+        self.bytes = w.kv_read_bytes()
+        self.desc = (f"{nseq} sequence(s) x {ctx} tokens, {groups} of {Hkv} kv heads "
+                     f"(x{g} q heads), head_dim {D}")
+
+    def step(self) -> float:
+        w, o = self.w, self.o
+        t0 = time.perf_counter()
+        o.reshape_and_cache(self.k_new, self.v_new, self.kc, self.vc, w.new_slots, w.num_blocks,
+                            16, 1, self.kv_dtype, self.sc, self.sc)
+        o.paged_attention_decode(self.q, self.kc, self.vc, w.block_tables, w.context_lens,
+                                 w.num_kv_heads, w.head_dim, 16, w.num_blocks, w.scale, 1,
+                                 self.kv_dtype, self.sc, self.sc)
+        return time.perf_counter() - t0
+
+
+def oracle_sample(w, budget_s: float) -> OracleSample:
+    """The largest sample (KV heads of one sequence, then whole sequences) whose
+    step takes about budget_s on one core."""
+    H, Hkv, D = w.num_heads, w.num_kv_heads, w.head_dim
+    ctx = int(w.context_lens.max())
+    probe = OracleSample(H, Hkv, D, ctx, w.kv_dtype, 1, 1)
+    per_group = min(probe.step(), probe.step())
+    groups = int(max(1, min(Hkv, budget_s / max(per_group, 1e-6))))
+    nseq = 1
+    if groups == Hkv:
+        nseq = int(max(1, min(w.num_seqs, budget_s / max(per_group * Hkv, 1e-6))))
+    return OracleSample(H, Hkv, D, ctx, w.kv_dtype, nseq, groups)
+
+
+# ---- main ----------------------------------------------------------------------------------
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    import workloads
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        return reference_arm(args, world)
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import paged_kv_cache_98_gb300 as pkv
+    from paged_kv_cache_98_gb300 import _build
+    if rank == 0 or world == 1:
+        _build.build()
+    if dist:
+        dist.barrier()
+    pkv.load()
+
+    def barrier():
+        if dist:
+            dist.barrier()
+
+    w = workloads.llama2_7b()
+    st = GpuStep(w, dev)
+    sampler = ClockSampler(local).start()
+    time.sleep(0.3)
+    res = st.timed(args.steps, args.warmup, barrier)
+    clocks = sampler.stop()
+    total = res["total_ms"]
+    if dist:
+        t = torch.tensor([total], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total = float(t.item())
+    if pkv.check_errors(st.err) != 0:
+        raise RuntimeError("device-side checks failed during the timed steps")
+    ms = total / args.steps
+    kv_bytes = w.kv_read_bytes()
+    tokens = int(w.context_lens.astype("int64").sum())
+    value = world * kv_bytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    dec_ms = res["decode_ms"]
+    achieved = kv_bytes / (dec_ms * 1e-3) / 1e9
+    e2e_ms, h2d, d2h = st.e2e(max(20, min(args.steps, 200)), 5)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) bf16 K/V/Q, block tables a seeded random permutation "
+                "of a pool 1.25x the demand",
+        "config": {
+            "workload": describe(w),
+            "num_seqs": w.num_seqs, "context": int(w.context_lens.max()),
+            "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "block_size": 16, "partition": 512, "pool_blocks": w.num_blocks,
+            "kv_bytes_per_step": kv_bytes,
+            "l2": "inputs larger than L2: 4.29 GB of K/V read per step vs 129 MB L2",
+            "parallelism": f"replicas x{world}",
+        },
+        "attended_tokens_per_s": round(world * tokens / (ms * 1e-3), 1),
+        "hbm_frac": round(value / world / peak, 4),
+        "roofline": {
+            "kernel": "paged decode attention (attention + log-sum-exp merge launches)",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+            "peak_kind": f"{peak_kind} HBM copy bandwidth",
+            "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": recorded_traffic("decode_llama2_7b"),
+            "algorithmic_bytes_per_launch": kv_bytes,
+            "decode_ms": round(dec_ms, 5), "write_ms": round(res["write_ms"], 5),
+        },
+        "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": st.launches_per_step() * args.steps,
+        "clocks": clocks,
+    }
+    del st
+    torch.cuda.empty_cache()
+    if not args.no_also:
+        line["also"] = other_workloads(dev, peak, barrier)
+    if rank == 0 and not args.no_cpu:
+        smp = oracle_sample(w, args.cpu_seconds)
+        secs = smp.step()
+        line["cpu_baseline"] = {"value": round(smp.bytes / secs / 1e9, 4), "unit": "GB/s",
+                                "cores": 1, "kind": "oracle", "sample": smp.desc,
+                                "seconds": round(secs, 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def other_workloads(dev, peak, barrier):
+    """The other named workloads, each timed the same way (fewer steps)."""
+    import torch
+
+    import workloads
+    out = {}
+    for name, steps in (("gqa70b_shared", 200), ("long_fp8", 100), ("mixed", 100)):
+        w = workloads.NAMED[name]()
+        st = GpuStep(w, dev)
+        res = st.timed(steps, 5, barrier)
+        ms = res["total_ms"] / steps
+        kvb = w.kv_read_bytes()
+        d = {"workload": describe(w), "ms_per_step": round(ms, 5),
+             "decode_ms": round(res["decode_ms"], 5),
+             "decode_GBps_logical": round(kvb / (res["decode_ms"] * 1e-3) / 1e9, 1),
+             "decode_frac_logical": round(kvb / (res["decode_ms"] * 1e-3) / 1e9 / peak, 4),
+             "kv_bytes_logical": kvb,
+             "attended_tokens_per_s": round(float(w.context_lens[w.decode_ids()].sum()) /
+                                            (res["decode_ms"] * 1e-3), 1)}
+        if name == "gqa70b_shared":
+            ub = unique_kv_bytes(w)
+            d["kv_bytes_unique"] = ub
+            d["decode_GBps_unique"] = round(ub / (res["decode_ms"] * 1e-3) / 1e9, 1)
+        if len(w.prefill_ids()):
+            flops = 0
+            for s in w.prefill_ids():
+                c, ql = int(w.context_lens[s]), int(w.q_lens[s])
+                keys = sum(c - ql + i + 1 for i in range(ql))
+                flops += 4 * w.num_heads * w.head_dim * keys
+            d["prefill_ms"] = round(res["prefill_ms"], 5)
+            d["prefill_tflops"] = round(flops / (res["prefill_ms"] * 1e-3) / 1e12, 2)
+            d["prefill_flops"] = flops
+        if pkv_errors(st):
+            d["device_errors"] = True
+        out[name] = d
+        del st
+        torch.cuda.empty_cache()
+    return out
+
+
+def pkv_errors(st) -> bool:
+    return st.pkv.check_errors(st.err) != 0
+
+
+def reference_arm(args, world):
+    """The oracle, as it stands, on one host core: each step a bounded sample of
+    the headline workload, sized so that the whole run takes a few minutes."""
+    import workloads
+    w = workloads.llama2_7b()
+    steps, warm = args.steps, args.warmup
+    budget = max(0.02, min(2.0, 150.0 / max(1, steps + warm)))
+    smp = oracle_sample(w, budget)
+    t0 = time.perf_counter()
+    times = []
+    for i in range(steps + warm):
+        dt = smp.step()
+        if i >= warm:
+            times.append(dt)
+    wall = time.perf_counter() - t0
+    sec = statistics.mean(times) if times else smp.step()
+    value = smp.bytes / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": round(sec * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded N(0,1) bf16 K/V/Q (CPU draw), scattered block tables",
+        "config": {"workload": describe(w), "sample_per_step": smp.desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": smp.desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "wall_s": round(wall, 1),
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

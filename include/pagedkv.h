@@ -1,0 +1,193 @@
+/*
+ * pagedkv.h -- C ABI of the paged KV-cache attention library (libpagedkv.so).
+ *
+ * One GPU (sm_103a).  The library allocates no device memory: the caller owns
+ * every buffer and passes device pointers.  Every compute call is asynchronous
+ * on the given CUDA stream (a cudaStream_t passed as void*; NULL is the legacy
+ * default stream), never synchronises, and never throws.  Arguments are
+ * validated on the host before anything is launched; a rejected call launches
+ * nothing and returns a negative pkv_status.
+ *
+ * Data model (sources: openeuler.csdn.net PagedAttention notes, "vLLM -
+ * PagedAttention", "Block Table 数据结构" and "Attention 计算时的 Block 映射
+ * （CUDA Kernel 伪代码）"; "第32讲 … Prefill vs Decode …", §3.4 GQA):
+ *   - the K cache and the V cache are each laid out
+ *       [num_blocks][num_kv_heads][block_size][head_dim]
+ *     so one (block, KV head) tile of block_size rows is contiguous;
+ *   - block_size is 16 tokens;
+ *   - block_tables is [num_seqs][max_blocks_per_seq] int32, row-major: entry j
+ *     of row s is the physical block holding tokens 16j .. 16j+15 of sequence s.
+ *     Entries past ceil(context_lens[s] / 16) are never read;
+ *   - a slot is physical_block * block_size + offset;
+ *   - query head h reads KV head h / (num_heads / num_kv_heads) (consecutive
+ *     groups);
+ *   - context_lens[s] counts every token of sequence s, including the new ones
+ *     whose K/V pkv_reshape_and_cache has already written;
+ *   - q and out are [rows][num_heads][head_dim] contiguous, in q_dtype.
+ *
+ * Supported: head_dim 64 or 128; block_size 16; num_heads a multiple of
+ * num_kv_heads with num_heads / num_kv_heads <= 16; q_dtype F16 or BF16;
+ * the cache dtype equal to q_dtype or FP8_E4M3.  Device pointers to caches,
+ * q, k, v and out must be 16-byte aligned.
+ *
+ * Device-side checks.  Each compute call takes `device_errors`, a device
+ * pointer to one uint32_t owned by the caller (or NULL to skip reporting).
+ * Kernels OR PKV_DEVERR_* bits into it when they meet a block id outside the
+ * pool, a context length beyond the table or the launch bounds, a slot outside
+ * the pool, or a device-side wait that gave up.  Such data is never read or
+ * written out of bounds: the offending access is clamped or skipped and the
+ * result of that row is unspecified.  pkv_check_errors reads and clears it.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = -1, /* a null pointer, a bad size, a misaligned pointer */
+  PKV_ERR_UNSUPPORTED = -2, /* a valid but unsupported shape or dtype combination */
+  PKV_ERR_WORKSPACE = -3,   /* workspace missing or smaller than the size function says */
+  PKV_ERR_CUDA = -4,        /* the CUDA runtime reported an error at launch */
+  PKV_ERR_DEVICE = -5,      /* pkv_check_errors: a device-side check failed */
+  PKV_ERR_TIMEOUT = -6      /* pkv_check_errors: a device-side wait gave up */
+} pkv_status;
+
+#define PKV_DEVERR_BLOCK_ID 0x1u    /* block table entry outside [0, num_blocks) */
+#define PKV_DEVERR_CONTEXT 0x2u     /* context/query length beyond the table or launch bounds */
+#define PKV_DEVERR_SLOT 0x4u        /* slot_mapping entry >= num_blocks * block_size */
+#define PKV_DEVERR_TIMEOUT 0x8u     /* a wait on an asynchronous copy or MMA gave up */
+
+/*
+ * Scatter new keys and values into the paged caches through a slot mapping.
+ * Source: devpress.csdn.net vLLM overview, "8、推理流程" (each layer's K and V
+ * are stored into the paged cache before attention reads it);
+ * openeuler.csdn.net PagedAttention notes, "Block Table 数据结构"
+ * (slot = physical_block * block_size + offset).
+ *
+ *   k, v          [num_tokens][num_kv_heads][head_dim], src_dtype (F16/BF16)
+ *   k_cache,
+ *   v_cache       caches as above, cache_dtype
+ *   slot_mapping  [num_tokens] int64; token t goes to slot slot_mapping[t].
+ *                 Negative entries are padding and are skipped.  Entries
+ *                 >= num_blocks * block_size are skipped and flagged
+ *                 PKV_DEVERR_SLOT.  Two tokens with one slot is a caller
+ *                 error (which one lands is unspecified).
+ *   cache_dtype   == src_dtype: the element bits are copied.
+ *                 FP8_E4M3: each element becomes E4M3(x / scale) with an IEEE
+ *                 float division, round to nearest even, saturating to +-448;
+ *                 scale is k_scale for K and v_scale for V (per tensor).
+ * num_tokens == 0 launches nothing and returns PKV_OK.
+ */
+int pkv_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                          const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                          int head_dim, int block_size, int num_blocks, pkv_dtype src_dtype,
+                          pkv_dtype cache_dtype, float k_scale, float v_scale,
+                          uint32_t* device_errors, void* stream);
+
+/*
+ * Bytes of device workspace pkv_paged_attention_decode needs for these
+ * arguments (0 when the context fits one partition).  partition_size 0 means
+ * the library's choice (the value the decode call would use).
+ */
+size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int head_dim,
+                                 int max_context_len, int partition_size);
+
+/*
+ * Decode attention: one query token per sequence attends every token of its
+ * context through the block table.
+ * Sources: "第32讲 … Prefill vs Decode …", §3.1 (softmax(q K^T / sqrt(d_k)) V
+ * over the cached K_{1:t}, V_{1:t}); openeuler.csdn.net PagedAttention notes,
+ * "Attention 计算时的 Block 映射（CUDA Kernel 伪代码）" (block_idx = i / 16,
+ * offset = i % 16, physical_block = block_table[block_idx]);
+ * devpress.csdn.net vLLM overview, "3、PagedAttention (3)" (per-block partial
+ * results combined) and "9、FlashAttention (4)" (running max and sum of
+ * exponentials, rescaled).
+ *
+ *   out   [num_seqs][num_heads][head_dim], q_dtype; row s, head h is
+ *         sum_t softmax_t(scale * q[s,h] . K[s,t]) V[s,t] over
+ *         t < context_lens[s]; a sequence with context 0 gets zeros.
+ *   q     [num_seqs][num_heads][head_dim], q_dtype
+ *   kv_dtype FP8_E4M3: K and V elements are decode(byte) * k_scale / v_scale;
+ *         otherwise the scales are ignored.
+ *   max_context_len  an upper bound of context_lens (sizes the launch; no
+ *         device-to-host read).  Longer contexts are flagged PKV_DEVERR_CONTEXT.
+ *   partition_size   tokens per split of the context (multiple of 16, at
+ *         most 512); 0 = the library's choice.  Contexts longer than one
+ *         partition are computed per partition into the workspace and
+ *         combined by a log-sum-exp merge.
+ *   workspace, workspace_bytes  device scratch of at least
+ *         pkv_decode_workspace_size(...) bytes, 256-byte aligned; may be NULL
+ *         when that size is 0.  Its contents need no initialisation.
+ */
+int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
+                               const void* v_cache, const int32_t* block_tables,
+                               const int32_t* context_lens, int num_seqs, int num_heads,
+                               int num_kv_heads, int head_dim, int block_size,
+                               int max_blocks_per_seq, int num_blocks, int max_context_len,
+                               float scale, pkv_dtype q_dtype, pkv_dtype kv_dtype,
+                               float k_scale, float v_scale, int partition_size,
+                               void* workspace, size_t workspace_bytes,
+                               uint32_t* device_errors, void* stream);
+
+/*
+ * Bytes of device workspace pkv_paged_attention_prefill_chunk needs.
+ */
+size_t pkv_prefill_workspace_size(int total_q, int num_heads, int head_dim,
+                                  int max_context_len, int max_q_len);
+
+/*
+ * Chunked-prefill attention: each sequence contributes its last q_len tokens
+ * as queries (a chunk of a prompt, or a single decode token), and each of
+ * them attends causally to the paged context before it and to itself.
+ * Sources: "第32讲 … Prefill vs Decode …", §5.4 (prompts cut into chunks of
+ * e.g. 512 tokens, each chunk attending the prior context); devpress.csdn.net
+ * vLLM overview, "9、FlashAttention (3)" (query blocks x key/value blocks).
+ *
+ *   q, out           [total_q][num_heads][head_dim], q_dtype
+ *   query_start_loc  [num_seqs + 1] int32, non-decreasing, [0] = 0,
+ *                    [num_seqs] = total_q; sequence s owns query rows
+ *                    query_start_loc[s] .. query_start_loc[s+1]-1.
+ *   The query at row query_start_loc[s] + i sits at absolute position
+ *   pos = context_lens[s] - q_len_s + i and attends keys 0..pos.
+ *   max_q_len        an upper bound of every q_len_s (sizes the launch).
+ *   Other arguments as for pkv_paged_attention_decode.
+ */
+int pkv_paged_attention_prefill_chunk(void* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_tables,
+                                      const int32_t* context_lens,
+                                      const int32_t* query_start_loc, int num_seqs,
+                                      int total_q, int max_q_len, int num_heads,
+                                      int num_kv_heads, int head_dim, int block_size,
+                                      int max_blocks_per_seq, int num_blocks,
+                                      int max_context_len, float scale, pkv_dtype q_dtype,
+                                      pkv_dtype kv_dtype, float k_scale, float v_scale,
+                                      void* workspace, size_t workspace_bytes,
+                                      uint32_t* device_errors, void* stream);
+
+/*
+ * Synchronises `stream`, reads the device error word, clears it, and returns
+ * PKV_OK, PKV_ERR_TIMEOUT (a wait gave up) or PKV_ERR_DEVICE (any other bit);
+ * PKV_ERR_CUDA if the stream reports an error.  *bits_out (may be NULL)
+ * receives the raw bits.
+ */
+int pkv_check_errors(uint32_t* device_errors, uint32_t* bits_out, void* stream);
+
+/* A static, human-readable name for a pkv_status value. */
+const char* pkv_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

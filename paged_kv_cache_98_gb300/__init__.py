@@ -1,0 +1,224 @@
+"""Paged KV-cache attention for one GB300 GPU: Python binding of libpagedkv.so.
+
+Each function here marshals torch tensors into the C ABI declared in
+include/pagedkv.h (Python ``X`` is C ``pkv_X``) and launches on the current
+torch CUDA stream.  All work runs in the library's CUDA kernels; there is no
+CPU or PyTorch fallback: if the library is missing the call raises.
+
+Tensor conventions:
+  q, out        [rows, num_heads, head_dim], float16 or bfloat16, contiguous
+  k, v          [num_tokens, num_kv_heads, head_dim], float16 or bfloat16
+  k_cache,
+  v_cache       [num_blocks, num_kv_heads, 16, head_dim]: float16/bfloat16, or
+                uint8 / float8_e4m3fn for an E4M3 cache
+  block_tables  [num_seqs, max_blocks_per_seq] int32
+  context_lens  [num_seqs] int32
+  slot_mapping  [num_tokens] int64
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "F16", "BF16", "FP8_E4M3", "PagedKVError", "library_path", "load", "reshape_and_cache",
+    "decode_workspace_size", "prefill_workspace_size", "paged_attention_decode",
+    "paged_attention_prefill_chunk", "check_errors", "status_string", "version",
+]
+
+F16, BF16, FP8_E4M3 = 0, 1, 2
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libpagedkv.so")
+_lib = None
+_lock = threading.Lock()
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+
+class PagedKVError(RuntimeError):
+    """A pkv_* call returned a negative status."""
+
+    def __init__(self, what: str, status: int):
+        super().__init__(f"{what} failed: {status_string(status)} ({status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Loads libpagedkv.so (built by __graft_entry__.build() or _build.build())."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"{_LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ "
+                    "as g; g.build()'); there is no fallback path")
+            lib = ctypes.CDLL(_LIB_PATH)
+            lib.pkv_version.restype = _I
+            lib.pkv_version.argtypes = []
+            lib.pkv_status_string.restype = ctypes.c_char_p
+            lib.pkv_status_string.argtypes = [_I]
+            lib.pkv_reshape_and_cache.restype = _I
+            lib.pkv_reshape_and_cache.argtypes = [_P] * 5 + [_I] * 7 + [_F, _F, _P, _P]
+            lib.pkv_decode_workspace_size.restype = _SZ
+            lib.pkv_decode_workspace_size.argtypes = [_I] * 5
+            lib.pkv_prefill_workspace_size.restype = _SZ
+            lib.pkv_prefill_workspace_size.argtypes = [_I] * 5
+            lib.pkv_paged_attention_decode.restype = _I
+            lib.pkv_paged_attention_decode.argtypes = (
+                [_P] * 6 + [_I] * 8 + [_F, _I, _I, _F, _F, _I, _P, _SZ, _P, _P])
+            lib.pkv_paged_attention_prefill_chunk.restype = _I
+            lib.pkv_paged_attention_prefill_chunk.argtypes = (
+                [_P] * 7 + [_I] * 10 + [_F, _I, _I, _F, _F, _P, _SZ, _P, _P])
+            lib.pkv_check_errors.restype = _I
+            lib.pkv_check_errors.argtypes = [_P, _P, _P]
+            _lib = lib
+    return _lib
+
+
+def version() -> int:
+    return load().pkv_version()
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().pkv_status_string(status).decode()
+    except Exception:
+        return "unknown"
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return F16
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return FP8_E4M3
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors must be on the CUDA device")
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def _check(what, rc):
+    if rc != 0:
+        raise PagedKVError(what, rc)
+
+
+def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, k_scale: float = 1.0,
+                      v_scale: float = 1.0, device_errors=None, stream=None):
+    """Writes k, v ([T, Hkv, D]) into the caches at slot_mapping ([T] int64)."""
+    _need_cuda(k, v, k_cache, v_cache, slot_mapping, device_errors)
+    T, hkv, d = k.shape
+    rc = load().pkv_reshape_and_cache(
+        _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), T, hkv, d,
+        k_cache.shape[2], k_cache.shape[0], _dtype_code(k), _dtype_code(k_cache), k_scale,
+        v_scale, _ptr(device_errors), _stream(stream))
+    _check("pkv_reshape_and_cache", rc)
+
+
+def decode_workspace_size(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,
+                          partition_size: int = 0) -> int:
+    return int(load().pkv_decode_workspace_size(num_seqs, num_heads, head_dim, max_context_len,
+                                                partition_size))
+
+
+def prefill_workspace_size(total_q: int, num_heads: int, head_dim: int, max_context_len: int,
+                           max_q_len: int) -> int:
+    return int(load().pkv_prefill_workspace_size(total_q, num_heads, head_dim, max_context_len,
+                                                 max_q_len))
+
+
+def _workspace(nbytes, workspace, device):
+    if nbytes == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                           num_kv_heads: int | None = None, max_context_len: int | None = None,
+                           k_scale: float = 1.0, v_scale: float = 1.0, partition_size: int = 0,
+                           workspace=None, device_errors=None, stream=None):
+    """Decode attention of q ([S, H, D]) over the paged caches into out.
+
+    max_context_len bounds context_lens; passing it avoids a device-to-host read.
+    workspace (uint8, >= decode_workspace_size bytes) is allocated if omitted.
+    """
+    _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, device_errors)
+    S, H, D = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    if num_kv_heads is not None and num_kv_heads != hkv:
+        raise ValueError("num_kv_heads does not match the cache shape")
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if S else 0
+    need = decode_workspace_size(S, H, D, max_context_len, partition_size)
+    ws, wsb = _workspace(need, workspace, q.device)
+    rc = load().pkv_paged_attention_decode(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        S, H, hkv, D, bs, block_tables.shape[1], nb, max_context_len, scale, _dtype_code(q),
+        _dtype_code(k_cache), k_scale, v_scale, partition_size, _ptr(ws), wsb,
+        _ptr(device_errors), _stream(stream))
+    _check("pkv_paged_attention_decode", rc)
+    return out
+
+
+def paged_attention_prefill_chunk(out, q, k_cache, v_cache, block_tables, context_lens,
+                                  query_start_loc, scale: float, max_q_len: int | None = None,
+                                  max_context_len: int | None = None, k_scale: float = 1.0,
+                                  v_scale: float = 1.0, workspace=None, device_errors=None,
+                                  stream=None):
+    """Causal chunked-prefill attention of q ([total_q, H, D]) into out."""
+    _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc,
+               device_errors)
+    TQ, H, D = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    S = context_lens.shape[0]
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if S else 0
+    if max_q_len is None:
+        max_q_len = int((query_start_loc[1:] - query_start_loc[:-1]).max().item()) if S else 0
+    need = prefill_workspace_size(TQ, H, D, max_context_len, max_q_len)
+    ws, wsb = _workspace(need, workspace, q.device)
+    rc = load().pkv_paged_attention_prefill_chunk(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        _ptr(query_start_loc), S, TQ, max_q_len, H, hkv, D, bs, block_tables.shape[1], nb,
+        max_context_len, scale, _dtype_code(q), _dtype_code(k_cache), k_scale, v_scale, _ptr(ws),
+        wsb, _ptr(device_errors), _stream(stream))
+    _check("pkv_paged_attention_prefill_chunk", rc)
+    return out
+
+
+def check_errors(device_errors, stream=None) -> int:
+    """Synchronises, reads and clears the device error word; returns its bits."""
+    bits = ctypes.c_uint32(0)
+    rc = load().pkv_check_errors(_ptr(device_errors), ctypes.byref(bits), _stream(stream))
+    if rc not in (0, -5, -6):
+        raise PagedKVError("pkv_check_errors", rc)
+    return bits.value

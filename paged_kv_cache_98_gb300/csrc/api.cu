@@ -1,0 +1,263 @@
+// C ABI of libpagedkv.so: argument validation and kernel dispatch.  The
+// declarations, data model and error conventions are in include/pagedkv.h.
+
+#include <cmath>
+#include <cstdint>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+constexpr int kDefaultPartition = 512;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is16bit(int dt) { return dt == PKV_F16 || dt == PKV_BF16; }
+
+int effective_partition(int partition_size, int max_context_len) {
+  int ps = partition_size == 0 ? kDefaultPartition : partition_size;
+  (void)max_context_len;
+  return ps;
+}
+
+int parts_for(int max_context_len, int partition) {
+  int n = (max_context_len + partition - 1) / partition;
+  return n < 1 ? 1 : n;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t split_workspace(size_t rows, int num_heads, int head_dim, int max_parts) {
+  if (max_parts <= 1) return 0;
+  const size_t heads = rows * (size_t)num_heads * (size_t)max_parts;
+  return round_up(heads * sizeof(float), 256) + round_up(heads * head_dim * sizeof(float), 256);
+}
+
+int pow2_at_least(int g) {
+  int p = 1;
+  while (p < g) p <<= 1;
+  return p;
+}
+
+// Checks shared by decode and prefill.
+int check_attention_args(const void* out, const void* q, const void* k_cache,
+                         const void* v_cache, const int32_t* block_tables,
+                         const int32_t* context_lens, int num_seqs, int num_heads,
+                         int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                         int num_blocks, int max_context_len, float scale, int q_dtype,
+                         int kv_dtype, float k_scale, float v_scale) {
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return PKV_ERR_INVALID_ARG;
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 ||
+      num_blocks <= 0 || max_context_len < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+  if (block_size != pkv::kBlockSize) return PKV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (num_heads / num_kv_heads > 16) return PKV_ERR_UNSUPPORTED;
+  if (!is16bit(q_dtype)) return PKV_ERR_UNSUPPORTED;
+  if (kv_dtype != q_dtype && kv_dtype != PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
+  if (kv_dtype == PKV_FP8_E4M3) {
+    if (!(k_scale > 0.0f) || !(v_scale > 0.0f) || !std::isfinite(k_scale) ||
+        !std::isfinite(v_scale))
+      return PKV_ERR_INVALID_ARG;
+  }
+  if ((long long)max_blocks_per_seq * pkv::kBlockSize > (1LL << 30)) return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+int run_attention(pkv::AttnParams& p, int q_dtype, int kv_dtype, int head_dim, float scale,
+                  float k_scale, float v_scale, void* workspace, size_t ws_need,
+                  size_t workspace_bytes, cudaStream_t stream) {
+  if (ws_need > 0) {
+    if (!workspace || workspace_bytes < ws_need) return PKV_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKV_ERR_INVALID_ARG;
+    const size_t heads = (size_t)p.num_rows * p.num_heads * p.max_parts;
+    p.lse = static_cast<float*>(workspace);
+    p.o_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                        round_up(heads * sizeof(float), 256));
+  } else {
+    p.lse = nullptr;
+    p.o_part = nullptr;
+  }
+  const bool fp8 = kv_dtype == PKV_FP8_E4M3;
+  p.q_scale = scale * pkv::kLog2e * (fp8 ? k_scale : 1.0f);
+  p.v_scale = fp8 ? v_scale : 1.0f;
+  const int g_pad = pow2_at_least(p.group);
+  int rc = pkv::launch_paged_attention_simt(p, q_dtype, kv_dtype, head_dim, g_pad, stream);
+  if (rc != PKV_OK) return rc;
+  if (p.max_parts > 1) rc = pkv::launch_lse_merge(p, q_dtype, head_dim, stream);
+  return rc;
+}
+
+}  // namespace
+
+namespace pkv {
+int launch_paged_attention_simt(const AttnParams& p, int q_dtype, int kv_dtype, int head_dim,
+                                int g_pad, cudaStream_t stream) {
+  if (q_dtype == PKV_F16)
+    return kv_dtype == PKV_FP8_E4M3 ? launch_simt_f16_e4m3(p, head_dim, g_pad, stream)
+                                    : launch_simt_f16_f16(p, head_dim, g_pad, stream);
+  return kv_dtype == PKV_FP8_E4M3 ? launch_simt_bf16_e4m3(p, head_dim, g_pad, stream)
+                                  : launch_simt_bf16_bf16(p, head_dim, g_pad, stream);
+}
+}  // namespace pkv
+
+extern "C" {
+
+int pkv_version(void) { return 100; }
+
+const char* pkv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_DEVICE: return "device-side check failed";
+    case PKV_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int pkv_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                          const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                          int head_dim, int block_size, int num_blocks, pkv_dtype src_dtype,
+                          pkv_dtype cache_dtype, float k_scale, float v_scale,
+                          uint32_t* device_errors, void* stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+  if (block_size != pkv::kBlockSize) return PKV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (!is16bit(src_dtype)) return PKV_ERR_UNSUPPORTED;
+  if (cache_dtype != src_dtype && cache_dtype != PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
+  if (cache_dtype == PKV_FP8_E4M3 &&
+      (!(k_scale > 0.0f) || !(v_scale > 0.0f) || !std::isfinite(k_scale) || !std::isfinite(v_scale)))
+    return PKV_ERR_INVALID_ARG;
+  return pkv::launch_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, num_tokens,
+                                       num_kv_heads, head_dim, num_blocks, src_dtype,
+                                       cache_dtype, k_scale, v_scale, device_errors,
+                                       static_cast<cudaStream_t>(stream));
+}
+
+size_t pkv_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                                 int partition_size) {
+  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
+  const int ps = effective_partition(partition_size, max_context_len);
+  if (ps <= 0) return 0;
+  return split_workspace((size_t)num_seqs, num_heads, head_dim, parts_for(max_context_len, ps));
+}
+
+int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, const int32_t* context_lens,
+                               int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                               int block_size, int max_blocks_per_seq, int num_blocks,
+                               int max_context_len, float scale, pkv_dtype q_dtype,
+                               pkv_dtype kv_dtype, float k_scale, float v_scale,
+                               int partition_size, void* workspace, size_t workspace_bytes,
+                               uint32_t* device_errors, void* stream) {
+  int rc = check_attention_args(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                num_heads, num_kv_heads, head_dim, block_size,
+                                max_blocks_per_seq, num_blocks, max_context_len, scale, q_dtype,
+                                kv_dtype, k_scale, v_scale);
+  if (rc != PKV_OK) return rc;
+  if (partition_size != 0 &&
+      (partition_size % pkv::kBlockSize != 0 || partition_size < pkv::kBlockSize ||
+       partition_size > 512))
+    return PKV_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PKV_OK;
+  const int ps = effective_partition(partition_size, max_context_len);
+  pkv::AttnParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.query_start_loc = nullptr;
+  p.num_seqs = num_seqs;
+  p.num_rows = num_seqs;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_heads / num_kv_heads;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.partition = ps;
+  p.max_parts = parts_for(max_context_len, ps);
+  if (p.max_parts > 16384) return PKV_ERR_UNSUPPORTED;
+  p.errors = device_errors;
+  const size_t need = split_workspace((size_t)num_seqs, num_heads, head_dim, p.max_parts);
+  return run_attention(p, q_dtype, kv_dtype, head_dim, scale, k_scale, v_scale, workspace, need,
+                       workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t pkv_prefill_workspace_size(int total_q, int num_heads, int head_dim, int max_context_len,
+                                  int max_q_len) {
+  (void)max_q_len;
+  if (total_q <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
+  return split_workspace((size_t)total_q, num_heads, head_dim,
+                         parts_for(max_context_len, kDefaultPartition));
+}
+
+int pkv_paged_attention_prefill_chunk(void* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_tables,
+                                      const int32_t* context_lens,
+                                      const int32_t* query_start_loc, int num_seqs, int total_q,
+                                      int max_q_len, int num_heads, int num_kv_heads,
+                                      int head_dim, int block_size, int max_blocks_per_seq,
+                                      int num_blocks, int max_context_len, float scale,
+                                      pkv_dtype q_dtype, pkv_dtype kv_dtype, float k_scale,
+                                      float v_scale, void* workspace, size_t workspace_bytes,
+                                      uint32_t* device_errors, void* stream) {
+  int rc = check_attention_args(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                num_heads, num_kv_heads, head_dim, block_size,
+                                max_blocks_per_seq, num_blocks, max_context_len, scale, q_dtype,
+                                kv_dtype, k_scale, v_scale);
+  if (rc != PKV_OK) return rc;
+  if (!query_start_loc || total_q < 0 || max_q_len < 0) return PKV_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_q == 0) return PKV_OK;
+  pkv::AttnParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.query_start_loc = query_start_loc;
+  p.num_seqs = num_seqs;
+  p.num_rows = total_q;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_heads / num_kv_heads;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.partition = kDefaultPartition;
+  p.max_parts = parts_for(max_context_len, kDefaultPartition);
+  if (p.max_parts > 16384) return PKV_ERR_UNSUPPORTED;
+  p.errors = device_errors;
+  const size_t need = split_workspace((size_t)total_q, num_heads, head_dim, p.max_parts);
+  return run_attention(p, q_dtype, kv_dtype, head_dim, scale, k_scale, v_scale, workspace, need,
+                       workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int pkv_check_errors(uint32_t* device_errors, uint32_t* bits_out, void* stream) {
+  if (!device_errors) return PKV_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+  uint32_t bits = 0;
+  if (cudaMemcpy(&bits, device_errors, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (cudaMemset(device_errors, 0, sizeof(uint32_t)) != cudaSuccess) return PKV_ERR_CUDA;
+  if (bits_out) *bits_out = bits;
+  if (bits & PKV_DEVERR_TIMEOUT) return PKV_ERR_TIMEOUT;
+  return bits ? PKV_ERR_DEVICE : PKV_OK;
+}
+
+}  // extern "C"

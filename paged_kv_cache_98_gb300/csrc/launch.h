@@ -1,0 +1,58 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+// One launch of the paged attention kernels.  A "row" is one query token:
+// a decode sequence (query_start_loc == nullptr, row = sequence) or one query
+// of a prefill chunk (row = index into q, its sequence found through
+// query_start_loc).
+struct AttnParams {
+  void* out;                      // [rows][num_heads][head_dim], q dtype
+  const void* q;                  // [rows][num_heads][head_dim], q dtype
+  const uint8_t* k_cache;         // [num_blocks][num_kv_heads][16][head_dim]
+  const uint8_t* v_cache;
+  const int32_t* block_tables;    // [num_seqs][max_blocks_per_seq]
+  const int32_t* context_lens;    // [num_seqs]
+  const int32_t* query_start_loc; // [num_seqs + 1] or nullptr (decode)
+  int num_seqs;
+  int num_rows;
+  int num_heads;
+  int num_kv_heads;
+  int group;                      // num_heads / num_kv_heads
+  int max_blocks_per_seq;
+  int num_blocks;
+  int partition;                  // tokens per partition (multiple of 16)
+  int max_parts;                  // partitions launched per row
+  float q_scale;                  // softmax scale * log2(e) (* k_scale for E4M3)
+  float v_scale;                  // 1, or v_scale for E4M3
+  float* o_part;                  // [rows][num_heads][max_parts][head_dim] (split only)
+  float* lse;                     // [rows][num_heads][max_parts], base-2 units (split only)
+  uint32_t* errors;               // device error word or nullptr
+};
+
+int launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                             const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                             int head_dim, int num_blocks, int src_dtype, int cache_dtype,
+                             float k_scale, float v_scale, uint32_t* errors,
+                             cudaStream_t stream);
+
+// CUDA-core paged attention (any group size up to 16) plus the merge of
+// partitions when p.max_parts > 1.  g_pad is the group size rounded up to a
+// power of two.
+int launch_paged_attention_simt(const AttnParams& p, int q_dtype, int kv_dtype, int head_dim,
+                                int g_pad, cudaStream_t stream);
+
+// Per-(q dtype, kv dtype) launchers, one translation unit each.
+int launch_simt_f16_f16(const AttnParams& p, int head_dim, int g_pad, cudaStream_t s);
+int launch_simt_f16_e4m3(const AttnParams& p, int head_dim, int g_pad, cudaStream_t s);
+int launch_simt_bf16_bf16(const AttnParams& p, int head_dim, int g_pad, cudaStream_t s);
+int launch_simt_bf16_e4m3(const AttnParams& p, int head_dim, int g_pad, cudaStream_t s);
+
+int launch_lse_merge(const AttnParams& p, int q_dtype, int head_dim, cudaStream_t stream);
+
+}  // namespace pkv

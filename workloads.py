@@ -123,7 +123,7 @@ def _assemble(name, r, ctx, q_lens, tables, seq_rows, num_src, fill_rows, fill_s
         bt[s, :len(t)] = t
     new_rows, new_slots = [], []
     for s in range(S):
-        pos = np.arange(ctx[s] - q_lens[s], ctx[s], dtype=np.int64)
+        pos = np.arange(max(0, ctx[s] - q_lens[s]), ctx[s], dtype=np.int64)
         new_rows.append(seq_rows[s][pos])
         new_slots.append(_slots(np.asarray(tables[s]), pos))
     return Workload(
@@ -157,7 +157,7 @@ def independent(name: str, seed: int, context_lens, H: int, Hkv: int, D: int, q_
         tables.append(t)
         rows = np.arange(base, base + c, dtype=np.int64)
         seq_rows.append(rows)
-        prior = c - q_lens[s]
+        prior = max(0, c - q_lens[s])
         fill_rows.append(rows[:prior])
         fill_slots.append(_slots(t, np.arange(prior)))
         base += c
