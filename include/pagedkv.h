@@ -138,6 +138,44 @@ int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
                                uint32_t* device_errors, void* stream);
 
 /*
+ * Decode attention that allocates nothing and takes no workspace.
+ * (The source pages have no counterpart: this entry point exists for callers
+ * of the library, not for the method.)
+ *
+ * For callers that cannot call cudaMalloc or hand over scratch memory: for
+ * example a host framework that owns all device memory through its own pool
+ * and forbids plugins from allocating, or a latency-critical loop that must
+ * not pay the implicit synchronisation of cudaMalloc/cudaFree.  It computes
+ * exactly what pkv_paged_attention_decode computes, with the same arguments
+ * minus the workspace, and keeps the split-K scratch in one fixed device
+ * array of PKV_DECODE_NOALLOC_SCRATCH_BYTES inside the library.
+ *
+ *   - The array is reserved on every GPU where this entry point is used and
+ *     stays reserved until the process exits.
+ *   - The first call on a device looks up the array's address (with that
+ *     device current); make that first call before any stream capture.
+ *   - Calls whose pkv_decode_workspace_size(...) exceeds
+ *     PKV_DECODE_NOALLOC_SCRATCH_BYTES are rejected with PKV_ERR_WORKSPACE
+ *     before anything is launched.
+ *   - All calls on a device share the one array, and it keeps the previous
+ *     call's contents.  Every byte a call reads is written earlier in that same
+ *     call, so nothing needs clearing.  Calls that overlap on the GPU (on
+ *     different streams, without ordering between them) race on the array and
+ *     give undefined results.
+ *   - No cudaMalloc, cudaFree or allocating library routine is called.
+ */
+#define PKV_DECODE_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_cache,
+                                       const void* v_cache, const int32_t* block_tables,
+                                       const int32_t* context_lens, int num_seqs,
+                                       int num_heads, int num_kv_heads, int head_dim,
+                                       int block_size, int max_blocks_per_seq, int num_blocks,
+                                       int max_context_len, float scale, pkv_dtype q_dtype,
+                                       pkv_dtype kv_dtype, float k_scale, float v_scale,
+                                       int partition_size, uint32_t* device_errors,
+                                       void* stream);
+
+/*
  * Bytes of device workspace pkv_paged_attention_prefill_chunk needs.
  */
 size_t pkv_prefill_workspace_size(int total_q, int num_heads, int head_dim,

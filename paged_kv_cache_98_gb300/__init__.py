@@ -26,7 +26,7 @@ import torch
 __all__ = [
     "F16", "BF16", "FP8_E4M3", "PagedKVError", "library_path", "load", "reshape_and_cache",
     "decode_workspace_size", "prefill_workspace_size", "paged_attention_decode",
-    "paged_attention_prefill_chunk", "check_errors", "status_string", "version",
+    "paged_attention_decode_noalloc", "paged_attention_prefill_chunk", "check_errors", "status_string", "version",
 ]
 
 F16, BF16, FP8_E4M3 = 0, 1, 2
@@ -79,6 +79,9 @@ def load():
             lib.pkv_paged_attention_prefill_chunk.restype = _I
             lib.pkv_paged_attention_prefill_chunk.argtypes = (
                 [_P] * 7 + [_I] * 10 + [_F, _I, _I, _F, _F, _P, _SZ, _P, _P])
+            lib.pkv_paged_attention_decode_noalloc.restype = _I
+            lib.pkv_paged_attention_decode_noalloc.argtypes = (
+                [_P] * 6 + [_I] * 8 + [_F, _I, _I, _F, _F, _I, _P, _P])
             lib.pkv_check_errors.restype = _I
             lib.pkv_check_errors.argtypes = [_P, _P, _P]
             _lib = lib
@@ -186,6 +189,25 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
         _dtype_code(k_cache), k_scale, v_scale, partition_size, _ptr(ws), wsb,
         _ptr(device_errors), _stream(stream))
     _check("pkv_paged_attention_decode", rc)
+    return out
+
+
+def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
+                                   scale: float, max_context_len: int, k_scale: float = 1.0,
+                                   v_scale: float = 1.0, partition_size: int = 0,
+                                   device_errors=None, stream=None):
+    """Decode attention with the library's fixed scratch array instead of a
+    workspace, for callers that may not allocate device memory (see
+    pkv_paged_attention_decode_noalloc in include/pagedkv.h)."""
+    _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, device_errors)
+    S, H, D = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    rc = load().pkv_paged_attention_decode_noalloc(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        S, H, hkv, D, bs, block_tables.shape[1], nb, max_context_len, scale, _dtype_code(q),
+        _dtype_code(k_cache), k_scale, v_scale, partition_size, _ptr(device_errors),
+        _stream(stream))
+    _check("pkv_paged_attention_decode_noalloc", rc)
     return out
 
 
