@@ -88,7 +88,11 @@ int run_attention(pkv::AttnParams& p, int q_dtype, int kv_dtype, int head_dim, f
   p.q_scale = scale * pkv::kLog2e * (fp8 ? k_scale : 1.0f);
   p.v_scale = fp8 ? v_scale : 1.0f;
   const int g_pad = pow2_at_least(p.group);
-  int rc = pkv::launch_paged_attention_simt(p, q_dtype, kv_dtype, head_dim, g_pad, stream);
+  int rc;
+  if (pkv::tc_decode_supported(p, q_dtype, kv_dtype, head_dim))
+    rc = pkv::launch_paged_decode_tc(p, q_dtype, stream);
+  else
+    rc = pkv::launch_paged_attention_simt(p, q_dtype, kv_dtype, head_dim, g_pad, stream);
   if (rc != PKV_OK) return rc;
   if (p.max_parts > 1) rc = pkv::launch_lse_merge(p, q_dtype, head_dim, stream);
   return rc;

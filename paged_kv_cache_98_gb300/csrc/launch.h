@@ -53,6 +53,11 @@ int launch_simt_f16_e4m3(const AttnParams& p, int head_dim, int g_pad, cudaStrea
 int launch_simt_bf16_bf16(const AttnParams& p, int head_dim, int g_pad, cudaStream_t s);
 int launch_simt_bf16_e4m3(const AttnParams& p, int head_dim, int g_pad, cudaStream_t s);
 
+// tcgen05 grouped-query decode (head_dim 128, 16-bit caches, 2..16 heads per
+// KV head, 512-token partitions, decode rows only).
+bool tc_decode_supported(const AttnParams& p, int q_dtype, int kv_dtype, int head_dim);
+int launch_paged_decode_tc(const AttnParams& p, int q_dtype, cudaStream_t stream);
+
 int launch_lse_merge(const AttnParams& p, int q_dtype, int head_dim, cudaStream_t stream);
 
 }  // namespace pkv
