@@ -48,6 +48,9 @@ def parse_args():
     ap.add_argument("--no-also", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workload", default="llama2_7b",
+                    help="named workload of the timed step (default: the LLaMA-2-7B-shaped "
+                         "decode); the others are for profiling one workload alone")
     return ap.parse_args()
 
 
@@ -61,28 +64,36 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def source_hash(files) -> str:
+    """sha256 (16 hex digits) of the named files under paged_kv_cache_98_gb300/csrc."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "paged_kv_cache_98_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode())
+    for name in sorted(files):
+        with open(os.path.join(ROOT, "paged_kv_cache_98_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(name: str):
-    """DRAM bytes per launch recorded by an ncu capture of the current kernel
-    sources (profiles/<name>.md, line 'traffic_bytes_per_launch: X src: H'), scaled
-    to a full launch; None when absent or taken on other sources."""
+    """DRAM bytes per full launch from an ncu capture summarised in
+    profiles/<name>.md (lines 'traffic_bytes_per_launch: X', 'src_files: a b ...',
+    'src_sha: H'); None when absent or when those kernel sources have changed."""
     path = os.path.join(ROOT, "profiles", name + ".md")
     try:
         text = open(path, encoding="utf-8").read()
     except OSError:
         return None
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+src:\s*([0-9a-f]+)", text)
-    if not m or m.group(2) != kernel_source_hash():
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    f = re.search(r"src_files:\s*(.+)", text)
+    h = re.search(r"src_sha:\s*([0-9a-f]+)", text)
+    if not (t and f and h):
         return None
-    return float(m.group(1))
+    try:
+        if source_hash(f.group(1).split()) != h.group(1):
+            return None
+    except OSError:
+        return None
+    return float(t.group(1))
 
 
 class ClockSampler:
@@ -413,7 +424,7 @@ def main():
         if dist:
             dist.barrier()
 
-    w = workloads.llama2_7b()
+    w = workloads.NAMED[args.workload]()
     st = GpuStep(w, dev)
     sampler = ClockSampler(local).start()
     time.sleep(0.3)
@@ -445,7 +456,7 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": {0: "f16", 1: "bf16"}[w.q_dtype] + ("+e4m3-kv" if w.kv_dtype == 2 else ""),
         "data": "synthetic: seeded N(0,1) bf16 K/V/Q, block tables a seeded random permutation "
                 "of a pool 1.25x the demand",
         "config": {
@@ -454,7 +465,8 @@ def main():
             "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
             "block_size": 16, "partition": 512, "pool_blocks": w.num_blocks,
             "kv_bytes_per_step": kv_bytes,
-            "l2": "inputs larger than L2: 4.29 GB of K/V read per step vs 129 MB L2",
+            "l2": f"inputs larger than L2: {kv_bytes / 1e9:.2f} GB of K/V read per step "
+                  "vs 129 MB L2",
             "parallelism": f"replicas x{world}",
         },
         "attended_tokens_per_s": round(world * tokens / (ms * 1e-3), 1),
@@ -476,7 +488,7 @@ def main():
     }
     del st
     torch.cuda.empty_cache()
-    if not args.no_also:
+    if not args.no_also and args.workload == "llama2_7b":
         line["also"] = other_workloads(dev, peak, barrier)
     if rank == 0 and not args.no_cpu:
         smp = oracle_sample(w, args.cpu_seconds)

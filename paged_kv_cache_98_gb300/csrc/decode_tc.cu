@@ -39,24 +39,38 @@
 namespace pkv {
 namespace {
 
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 224;
 constexpr int kTileKeys = 128;
 constexpr int kPart = 512;
 constexpr int kTilesPerPart = kPart / kTileKeys;
 constexpr int kD = 128;
-constexpr int kStages = 5;
 constexpr int kStageBytes = kTileKeys * kD * 2;  // 32 KB
 constexpr int kHalfBytes = kStageBytes / 2;      // 16 KB: 128 rows x 128 B
-constexpr int kQBytes = 16 * kD * 2;             // 4 KB: 2 halves x 16 rows x 128 B
-constexpr int kPBytes = 16 * kPart * 2;          // 16 KB: P[16 heads][512 keys]
-constexpr int kPGroupStride = (kPart / 8) * 128;  // 8 KB between 8-head groups
+constexpr int kPGroupStride = (kPart / 8) * 128;  // 8 KB between 8-head groups of P
 constexpr int kTmemCols = 256;                    // two items x (64 S + 16 O, padded)
-constexpr int kMaxSeqs = 2048;                    // sequences per launch on this path
+constexpr int kMaxSeqs = 1024;                    // sequences per launch (host chunks more)
 
+// Layout for groups of up to 8 (G16 false) or up to 16 (G16 true) query heads.
+// The MMA always has N = 16; with at most 8 heads, Q and P keep 8 rows and the
+// descriptors' 8-row group stride is 0, so rows 8-15 alias rows 0-7 (their
+// products are never read).  The shared memory saved buys a sixth ring stage.
+template <bool G16>
+struct Layout {
+  static constexpr int kStages = G16 ? 5 : 6;
+  static constexpr int kRows = G16 ? 16 : 8;               // Q / P rows held
+  static constexpr int kQHalf = kRows * 128;               // one 64-dim half of Q
+  static constexpr int kQBytes = 2 * kQHalf;
+  static constexpr int kQSbo = G16 ? 1024 : 0;
+  static constexpr int kPBytes = kRows * kPart * 2;
+  static constexpr int kPSbo = G16 ? kPGroupStride : 0;
+};
+
+template <bool G16>
 struct Smem {
+  static constexpr int kStages = Layout<G16>::kStages;
   uint8_t ring[kStages][kStageBytes];
-  uint8_t q[2][kQBytes];
-  uint8_t pmat[2][kPBytes];
+  uint8_t q[2][Layout<G16>::kQBytes];
+  uint8_t pmat[2][Layout<G16>::kPBytes];
   float stat_m[2][16];
   float stat_l[2][16];
   float red_max[4][16];
@@ -68,6 +82,7 @@ struct Smem {
   uint64_t s_ready[2];
   uint64_t p_ready[2];
   uint64_t o_ready[2];
+  uint64_t v_fixed[2];
   uint64_t mma_done;
   int seq_keys[kMaxSeqs];       // clamped context length of each sequence
   int seq_start[kMaxSeqs + 1];  // prefix sum of partitions per sequence
@@ -84,7 +99,8 @@ struct Item {
 // Items are the non-empty (sequence, partition) pairs in sequence order, each
 // split over the KV heads (KV head fastest): item k has KV head k % Hkv and
 // pair k / Hkv.  Consecutive items read neighbouring (block, head) tiles.
-__device__ __forceinline__ bool next_item(const AttnParams& p, const Smem& sm, int& idx,
+template <class SM>
+__device__ __forceinline__ bool next_item(const AttnParams& p, const SM& sm, int& idx,
                                           int total, Item& it) {
   if (idx >= total) return false;
   const int k = idx;
@@ -137,14 +153,18 @@ __device__ __forceinline__ bool all_softmax(bool ok) {
   return r != 0;
 }
 
-template <class QT>
+template <class QT, bool G16>
 __global__ void __launch_bounds__(kTcThreads, 1)
     paged_decode_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
                            const __grid_constant__ CUtensorMap tm_q, int kv_rows) {
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                      ~uintptr_t(1023));
+  using L = Layout<G16>;
+  constexpr int kStages = L::kStages;
+  constexpr int kQBytes = L::kQBytes;
+  constexpr int kPBytes = L::kPBytes;
+  Smem<G16>& sm = *reinterpret_cast<Smem<G16>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool split = p.max_parts > 1;
   constexpr uint32_t kAB = std::is_same<QT, BF16>::value ? 1u : 0u;
@@ -163,6 +183,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&sm.s_ready[b], 1);
       mbar_init(&sm.p_ready[b], 1);
       mbar_init(&sm.o_ready[b], 1);
+      mbar_init(&sm.v_fixed[b], 1);
     }
     mbar_init(&sm.mma_done, 1);
     sm.abort = 0;
@@ -244,14 +265,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_arrive_expect_tx(&sm.q_full[b], kQBytes);
           const int row = x.seq * p.num_heads + x.kvh * p.group;
           tc::tma_load_2d(&sm.q[b][0], &tm_q, 0, row, &sm.q_full[b]);
-          tc::tma_load_2d(&sm.q[b][kQBytes / 2], &tm_q, 64, row, &sm.q_full[b]);
+          tc::tma_load_2d(&sm.q[b][L::kQHalf], &tm_q, 64, row, &sm.q_full[b]);
         }
       }
       return __shfl_sync(kFull, (int)good, 0) != 0;
     };
-    auto load_tiles = [&](const Item& x, const CUtensorMap* map) -> bool {
+    // Row of block `lane` of an item's partition in the [block][kv head][16]
+    // row space of the caches (past the end when the block is not part of it).
+    auto block_row = [&](const Item& x) -> int {
       const int nblk = (x.n + kBlockSize - 1) / kBlockSize;
-      int row = kv_rows;  // past the end: the box reads zeros
+      int row = kv_rows;
       if (lane < nblk) {
         const int blk = __ldg(p.block_tables + (size_t)x.seq * p.max_blocks_per_seq +
                               x.part * (kPart / kBlockSize) + lane);
@@ -260,6 +283,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         else
           flag_error(p.errors, PKV_DEVERR_BLOCK_ID);
       }
+      return row;
+    };
+    auto load_tiles = [&](const Item& x, int row, const CUtensorMap* map) -> bool {
       for (int t = 0; t < x.ntiles; ++t, ++pos) {
         const int st = pos % kStages;
         bool good = true;
@@ -278,14 +304,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       return true;
     };
+    Item nxt2;
     bool has = next_item(p, sm, idx, total, cur);
-    if (has) ok = load_q(cur, 0) && load_tiles(cur, &tm_k);
+    int row_cur = has ? block_row(cur) : kv_rows;
+    if (has) ok = load_q(cur, 0) && load_tiles(cur, row_cur, &tm_k);
+    bool has_n = has && next_item(p, sm, idx, total, nxt);
+    int row_nxt = has_n ? block_row(nxt) : kv_rows;
     while (has && ok) {
-      const bool has_n = next_item(p, sm, idx, total, nxt);
-      if (has_n) ok = load_q(nxt, it + 1) && load_tiles(nxt, &tm_k);
-      if (ok) ok = load_tiles(cur, &tm_v);
+      // block rows are read one item ahead of their first use
+      const bool has_n2 = has_n && next_item(p, sm, idx, total, nxt2);
+      const int row_nxt2 = has_n2 ? block_row(nxt2) : kv_rows;
+      if (has_n) ok = load_q(nxt, it + 1) && load_tiles(nxt, row_nxt, &tm_k);
+      if (ok) ok = load_tiles(cur, row_cur, &tm_v);
       cur = nxt;
+      row_cur = row_nxt;
       has = has_n;
+      nxt = nxt2;
+      row_nxt = row_nxt2;
+      has_n = has_n2;
       ++it;
     }
     if (!ok && lane == 0) {
@@ -316,7 +352,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t off = (kk & 3) * 32u;
             const uint64_t a = tc::smem_desc(ka + (kk >> 2) * kHalfBytes + off, 16, 1024,
                                              tc::kLayoutSw128);
-            const uint64_t bq = tc::smem_desc(qa + (kk >> 2) * (kQBytes / 2) + off, 16, 1024,
+            const uint64_t bq = tc::smem_desc(qa + (kk >> 2) * L::kQHalf + off, 16, L::kQSbo,
                                               tc::kLayoutSw128);
             tc::mma_f16(tmem + b * 128 + t * 16, a, bq, kIdescS, kk > 0);
           }
@@ -329,6 +365,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       auto mma_pv = [&](const Item& x, int k) -> bool {
         const int b = k & 1;
         if (!wait_bar(&sm.p_ready[b], (k >> 1) & 1, abort)) return false;
+        if (!wait_bar(&sm.v_fixed[b], (k >> 1) & 1, abort)) return false;
         tc::fence_after_sync();
         const uint32_t pa = smem_u32(&sm.pmat[b][0]);
         for (int t = 0; t < x.ntiles; ++t, ++pos) {
@@ -341,7 +378,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint64_t a = tc::smem_desc(va + kk * (16 * 128), kHalfBytes, 1024,
                                              tc::kLayoutSw128);
             const uint64_t bp = tc::smem_desc(pa + (t * (kTileKeys / 8) + kk * 2) * 128, 128,
-                                              kPGroupStride, tc::kLayoutNone);
+                                              L::kPSbo, tc::kLayoutNone);
             tc::mma_f16(tmem + b * 128 + 64, a, bp, kIdescO, (t | kk) != 0);
           }
           tc::mma_commit(&sm.empty[st]);
@@ -364,6 +401,65 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::mma_commit(&sm.mma_done);
       mbar_wait(&sm.mma_done, 0, 100000000ull);
     }
+  } else if (warp == 6) {
+    // ---- V tail fixer -------------------------------------------------------------------
+    // V rows past the context in a partial last block hold whatever the pool
+    // had there; their P is zero, but 0 * NaN is NaN inside the MMA, so they
+    // are zeroed in shared memory once the tile has landed.  The MMA issuer
+    // waits for this warp's signal before the item's V products.
+    int idx = blockIdx.x;
+    uint32_t pos = 0;
+    Item cur, nxt;
+    int it = 0;
+    bool ok = true;
+    bool has = next_item(p, sm, idx, total, cur);
+    if (has) pos = cur.ntiles;
+    while (has && ok) {
+      const bool has_n = next_item(p, sm, idx, total, nxt);
+      const int b = it & 1;
+      // ring position of this item's last V tile (the producer's order: K of
+      // the next item, then V of this one)
+      if (has_n) pos += nxt.ntiles;
+      const uint32_t v_last = pos + cur.ntiles - 1;
+      pos += cur.ntiles;
+      bool good = true;
+      if (lane == 0) {
+        // at most one item ahead of the MMA issuer: item it-2 has been multiplied
+        if (it >= 2) good = wait_bar(&sm.o_ready[b], ((it - 2) >> 1) & 1, abort);
+      }
+      const int tail = cur.n & (kBlockSize - 1);
+      if (good && tail && lane == 0) {
+        // Once the producer has issued position v_last, every earlier use of
+        // that stage has completed, so the parity below names this use.
+        const uint64_t t0 = globaltimer_ns();
+        while (*reinterpret_cast<volatile uint32_t*>(&sm.issued) <= v_last) {
+          if (*abort || globaltimer_ns() - t0 > 2000000000ull) {
+            *abort = 1;
+            good = false;
+            break;
+          }
+        }
+        if (good) good = wait_bar(&sm.full[v_last % kStages], (v_last / kStages) & 1, abort);
+      }
+      ok = __shfl_sync(kFull, (int)good, 0) != 0;
+      if (!ok) break;
+      if (tail) {
+        const int jb = ((cur.n - 1) % kTileKeys) / kBlockSize;  // block within the tile
+        const int rows = kBlockSize - tail;
+        uint8_t* base = &sm.ring[v_last % kStages][0] + (jb * kBlockSize + tail) * 128;
+        for (int i = lane; i < rows * 2 * 8; i += 32) {
+          const int half = i / (rows * 8), r = (i / 8) % rows, c = i % 8;
+          reinterpret_cast<uint4*>(base + half * kHalfBytes + r * 128)[c] = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.v_fixed[b]);
+      cur = nxt;
+      has = has_n;
+      ++it;
+    }
+    if (!ok && lane == 0) flag_error(p.errors, PKV_DEVERR_TIMEOUT);
   } else {
     // ---- softmax + epilogue (warps 0-3, thread = TMEM lane) ---------------------------
     const int tid = threadIdx.x;  // 0..127
@@ -380,11 +476,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     int idx = blockIdx.x;
-    uint32_t pos = 0;
     Item cur, nxt, prev;
     int it = 0;
     bool has = next_item(p, sm, idx, total, cur);
-    if (has) pos = cur.ntiles;
 
     auto epilogue = [&](const Item& x, int k) -> bool {
       const int b = k & 1;
@@ -399,7 +493,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int nparts = (x.keys + kPart - 1) / kPart;
       const bool direct = !split || nparts == 1;
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
+      for (int h = 0; h < L::kRows; ++h) {
         if (h < p.group) {
           const float val = o[h] * (p.v_scale / sm.stat_l[b][h]);
           const size_t head = (size_t)x.seq * p.num_heads + (size_t)x.kvh * p.group + h;
@@ -419,12 +513,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     while (has) {
       const bool has_n = next_item(p, sm, idx, total, nxt);
       const int b = it & 1;
-      // ring position of this item's last V tile (the producer's order: K of
-      // the next item, then V of this one)
-      if (has_n) pos += nxt.ntiles;
-      const uint32_t v_last = pos + cur.ntiles - 1;
-      pos += cur.ntiles;
-
       ok = all_softmax(wait_bar(&sm.s_ready[b], (it >> 1) & 1, abort));
       if (!ok) break;
       tc::fence_after_sync();
@@ -436,18 +524,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // running max per head over this thread's keys, then over the CTA
       float mx[16];
 #pragma unroll
-      for (int h = 0; h < 16; ++h) mx[h] = -INFINITY;
+      for (int h = 0; h < L::kRows; ++h) mx[h] = -INFINITY;
 #pragma unroll
       for (int t = 0; t < kTilesPerPart; ++t) {
         const bool valid = t < cur.ntiles && t * kTileKeys + tid < cur.n;
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
+        for (int h = 0; h < L::kRows; ++h) {
           s[t][h] = valid ? s[t][h] * qs : -INFINITY;
           mx[h] = fmaxf(mx[h], s[t][h]);
         }
       }
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
+      for (int h = 0; h < L::kRows; ++h) {
         if (h < p.group) {
 #pragma unroll
           for (int o = 16; o; o >>= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], o));
@@ -457,7 +545,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::named_sync(1, 128);
       float sum[16];
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
+      for (int h = 0; h < L::kRows; ++h) {
         sum[h] = 0.0f;
         if (h < p.group)
           mx[h] = fmaxf(fmaxf(sm.red_max[0][h], sm.red_max[1][h]),
@@ -471,7 +559,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int key = t * kTileKeys + tid;
           uint8_t* col = pm + (key >> 3) * 128 + (key & 7) * 2;
 #pragma unroll
-          for (int h = 0; h < 16; ++h) {
+          for (int h = 0; h < L::kRows; ++h) {
             if (h < p.group) {
               const float e = fast_exp2(s[t][h] - mx[h]);
               sum[h] += e;
@@ -483,51 +571,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
+      for (int h = 0; h < L::kRows; ++h) {
         if (h < p.group) {
 #pragma unroll
           for (int o = 16; o; o >>= 1) sum[h] += __shfl_xor_sync(kFull, sum[h], o);
           if (lane == 0) sm.red_sum[warp][h] = sum[h];
         }
       }
-      // V rows past the context in the last block must not be NaN/Inf garbage:
-      // their P is zero, but 0 * NaN is NaN inside the MMA.
-      const int tail = cur.n & (kBlockSize - 1);
-      bool vok = true;
-      if (tail) {
-        // Once the producer has issued position v_last, every earlier use of
-        // that stage has completed, so the parity below names this use.
-        const uint64_t t0 = globaltimer_ns();
-        while (*reinterpret_cast<volatile uint32_t*>(&sm.issued) <= v_last) {
-          if (*abort || globaltimer_ns() - t0 > 2000000000ull) {
-            *abort = 1;
-            vok = false;
-            break;
-          }
-        }
-        if (vok) vok = wait_bar(&sm.full[v_last % kStages], (v_last / kStages) & 1, abort);
-        if (vok) {
-          const int jb = ((cur.n - 1) % kTileKeys) / kBlockSize;  // block within the tile
-          const int rows = kBlockSize - tail;
-          uint8_t* base = &sm.ring[v_last % kStages][0] + (jb * kBlockSize + tail) * 128;
-          for (int i = tid; i < rows * 2 * 8; i += 128) {
-            const int half = i / (rows * 8), r = (i / 8) % rows, c = i % 8;
-            reinterpret_cast<uint4*>(base + half * kHalfBytes + r * 128)[c] = make_uint4(0, 0, 0, 0);
-          }
-        }
-      }
-      ok = all_softmax(vok);
-      if (!ok) break;
+      fence_proxy_async_smem();
+      tc::fence_before_sync();
+      tc::named_sync(1, 128);  // P complete; every warp's partial sums written
+      if (tid == 0) mbar_arrive(&sm.p_ready[b]);
+      // read by this item's epilogue, after the next item's barriers
       if (tid < 16 && tid < p.group) {
         sm.stat_m[b][tid] = fmaxf(fmaxf(sm.red_max[0][tid], sm.red_max[1][tid]),
                                   fmaxf(sm.red_max[2][tid], sm.red_max[3][tid]));
         sm.stat_l[b][tid] =
             (sm.red_sum[0][tid] + sm.red_sum[1][tid]) + (sm.red_sum[2][tid] + sm.red_sum[3][tid]);
       }
-      fence_proxy_async_smem();
-      tc::fence_before_sync();
-      tc::named_sync(1, 128);
-      if (tid == 0) mbar_arrive(&sm.p_ready[b]);
 
       if (have_prev) {
         ok = epilogue(prev, it - 1);
@@ -566,13 +627,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Rows of 128 16-bit elements, boxes of 64 columns x 16 rows, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, bool bf16) {
+// Rows of 128 16-bit elements, boxes of 64 columns x box_rows rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, bool bf16, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-  cuuint32_t box[2] = {64, 16};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                   const_cast<void*>(base), dims, strides, box, estr,
@@ -592,17 +653,16 @@ int sm_count() {
   return n;
 }
 
-template <class QT>
+template <class QT, bool G16>
 int launch_tc_typed(const AttnParams& p, cudaStream_t stream) {
   const bool bf16 = std::is_same<QT, BF16>::value;
   const uint64_t kv_rows = (uint64_t)p.num_blocks * p.num_kv_heads * kBlockSize;
-  CUtensorMap tk, tv, tq;
-  if (!make_map(&tk, p.k_cache, kv_rows, bf16) || !make_map(&tv, p.v_cache, kv_rows, bf16) ||
-      !make_map(&tq, p.q, (uint64_t)p.num_rows * p.num_heads, bf16))
+  CUtensorMap tk, tv;
+  if (!make_map(&tk, p.k_cache, kv_rows, bf16, 16) || !make_map(&tv, p.v_cache, kv_rows, bf16, 16))
     return PKV_ERR_CUDA;
-  const size_t smem = sizeof(Smem) + 1024;
-  static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory budget of one CTA");
-  auto kern = paged_decode_tc_kernel<QT>;
+  const size_t smem = sizeof(Smem<G16>) + 1024;
+  static_assert(sizeof(Smem<G16>) + 1024 <= 232448, "shared memory budget of one CTA");
+  auto kern = paged_decode_tc_kernel<QT, G16>;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -610,12 +670,32 @@ int launch_tc_typed(const AttnParams& p, cudaStream_t stream) {
       return PKV_ERR_CUDA;
     configured = true;
   }
-  const long long items = (long long)p.num_rows * p.num_kv_heads * p.max_parts;
-  int grid = sm_count();
-  if (items < grid) grid = (int)items;
-  if (grid < 1) grid = 1;
-  kern<<<grid, kTcThreads, smem, stream>>>(p, tk, tv, tq, (int)kv_rows);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  using OutT = typename QT::T;
+  // launches of at most kMaxSeqs sequences each (their rows are independent)
+  for (int r0 = 0; r0 < p.num_rows; r0 += kMaxSeqs) {
+    AttnParams c = p;
+    c.num_rows = p.num_rows - r0 < kMaxSeqs ? p.num_rows - r0 : kMaxSeqs;
+    c.num_seqs = c.num_rows;
+    const size_t head0 = (size_t)r0 * p.num_heads;
+    c.out = static_cast<OutT*>(p.out) + head0 * kD;
+    c.q = static_cast<const OutT*>(p.q) + head0 * kD;
+    c.block_tables = p.block_tables + (size_t)r0 * p.max_blocks_per_seq;
+    c.context_lens = p.context_lens + r0;
+    if (p.lse) {
+      c.lse = p.lse + head0 * p.max_parts;
+      c.o_part = p.o_part + head0 * p.max_parts * kD;
+    }
+    CUtensorMap tq;
+    if (!make_map(&tq, c.q, (uint64_t)c.num_rows * p.num_heads, bf16, Layout<G16>::kRows))
+      return PKV_ERR_CUDA;
+    const long long items = (long long)c.num_rows * p.num_kv_heads * p.max_parts;
+    int grid = sm_count();
+    if (items < grid) grid = (int)items;
+    if (grid < 1) grid = 1;
+    kern<<<grid, kTcThreads, smem, stream>>>(c, tk, tv, tq, (int)kv_rows);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
 }
 
 }  // namespace
@@ -624,7 +704,6 @@ bool tc_decode_supported(const AttnParams& p, int q_dtype, int kv_dtype, int hea
   if (head_dim != kD || kv_dtype != q_dtype) return false;
   if (p.query_start_loc != nullptr || p.partition != kPart) return false;
   if (p.group < 2 || p.group > 16) return false;
-  if (p.num_rows > kMaxSeqs) return false;
   const uint64_t kv_rows = (uint64_t)p.num_blocks * p.num_kv_heads * kBlockSize;
   if (kv_rows + 16 >= (1ull << 31)) return false;
   if ((uint64_t)p.num_rows * p.num_heads + 16 >= (1ull << 31)) return false;
@@ -633,7 +712,10 @@ bool tc_decode_supported(const AttnParams& p, int q_dtype, int kv_dtype, int hea
 }
 
 int launch_paged_decode_tc(const AttnParams& p, int q_dtype, cudaStream_t stream) {
-  return q_dtype == PKV_BF16 ? launch_tc_typed<BF16>(p, stream) : launch_tc_typed<F16>(p, stream);
+  const bool g16 = p.group > 8;
+  if (q_dtype == PKV_BF16)
+    return g16 ? launch_tc_typed<BF16, true>(p, stream) : launch_tc_typed<BF16, false>(p, stream);
+  return g16 ? launch_tc_typed<F16, true>(p, stream) : launch_tc_typed<F16, false>(p, stream);
 }
 
 }  // namespace pkv

@@ -317,3 +317,17 @@ def test_full_mixed_sampled():
                                          w.num_kv_heads, w.head_dim, 16, nb, w.scale, BF16, BF16)
     got = pout[512:1024].float().cpu().numpy()
     check_close(got, ref, tol(w), "mixed prefill")
+
+
+def test_decode_many_sequences_chunked_launches():
+    # more sequences than one tensor-core launch takes: the host splits them
+    r = workloads.rng(91)
+    ctx = r.integers(0, 700, size=1100)
+    w = workloads.independent("many", 91, ctx, 8, 2, 128, BF16, BF16)
+    run_case(w)
+
+
+@pytest.mark.parametrize("g", [9, 12, 16])
+def test_decode_wide_groups(g):
+    w = workloads.independent("wide", 4000 + g, [1, 129, 700, 1600], g, 1, 128, F16, F16)
+    run_case(w)

@@ -272,9 +272,16 @@ def long_fp8(seed: int = 4, num_seqs: int = 8, context: int = 131072) -> Workloa
                        BF16, E4M3, partition_size=512)
 
 
+def llama2_7b_x16(seed: int = 1) -> Workload:
+    """The LLaMA-2-7B decode shape with 16 sequences (1.07 GB of K/V): a smaller
+    case of the same kernel for detailed profiling."""
+    return llama2_7b(seed, num_seqs=16)
+
+
 NAMED = {
     "tiny": tiny,
     "llama2_7b": llama2_7b,
+    "llama2_7b_x16": llama2_7b_x16,
     "gqa70b_shared": gqa70b_shared,
     "mixed": mixed,
     "long_fp8": long_fp8,
