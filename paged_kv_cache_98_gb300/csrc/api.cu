@@ -246,6 +246,13 @@ int pkv_paged_attention_prefill_chunk(void* out, const void* q, const void* k_ca
   p.max_parts = parts_for(max_context_len, kDefaultPartition);
   if (p.max_parts > 16384) return PKV_ERR_UNSUPPORTED;
   p.errors = device_errors;
+  if (pkv::tc_prefill_supported(p, q_dtype, kv_dtype, head_dim)) {
+    // tensor-core path: one pass over the keys per tile, no workspace
+    const bool fp8 = kv_dtype == PKV_FP8_E4M3;
+    p.q_scale = scale * pkv::kLog2e * (fp8 ? k_scale : 1.0f);
+    p.v_scale = fp8 ? v_scale : 1.0f;
+    return pkv::launch_prefill_tc(p, q_dtype, total_q, static_cast<cudaStream_t>(stream));
+  }
   const size_t need = split_workspace((size_t)total_q, num_heads, head_dim, p.max_parts);
   return run_attention(p, q_dtype, kv_dtype, head_dim, scale, k_scale, v_scale, workspace, need,
                        workspace_bytes, static_cast<cudaStream_t>(stream));

@@ -613,52 +613,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // ---- host side ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-// Rows of 128 16-bit elements, boxes of 64 columns x box_rows rows, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, bool bf16, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                  const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
-
 template <class QT, bool G16>
 int launch_tc_typed(const AttnParams& p, cudaStream_t stream) {
   const bool bf16 = std::is_same<QT, BF16>::value;
   const uint64_t kv_rows = (uint64_t)p.num_blocks * p.num_kv_heads * kBlockSize;
   CUtensorMap tk, tv;
-  if (!make_map(&tk, p.k_cache, kv_rows, bf16, 16) || !make_map(&tv, p.v_cache, kv_rows, bf16, 16))
+  if (!make_map_2d(&tk, p.k_cache, kv_rows, bf16, 16) || !make_map_2d(&tv, p.v_cache, kv_rows, bf16, 16))
     return PKV_ERR_CUDA;
   const size_t smem = sizeof(Smem<G16>) + 1024;
   static_assert(sizeof(Smem<G16>) + 1024 <= 232448, "shared memory budget of one CTA");
@@ -686,7 +646,7 @@ int launch_tc_typed(const AttnParams& p, cudaStream_t stream) {
       c.o_part = p.o_part + head0 * p.max_parts * kD;
     }
     CUtensorMap tq;
-    if (!make_map(&tq, c.q, (uint64_t)c.num_rows * p.num_heads, bf16, Layout<G16>::kRows))
+    if (!make_map_2d(&tq, c.q, (uint64_t)c.num_rows * p.num_heads, bf16, Layout<G16>::kRows))
       return PKV_ERR_CUDA;
     const long long items = (long long)c.num_rows * p.num_kv_heads * p.max_parts;
     int grid = sm_count();
@@ -708,7 +668,7 @@ bool tc_decode_supported(const AttnParams& p, int q_dtype, int kv_dtype, int hea
   if (kv_rows + 16 >= (1ull << 31)) return false;
   if ((uint64_t)p.num_rows * p.num_heads + 16 >= (1ull << 31)) return false;
   if ((long long)p.num_rows * p.num_kv_heads * p.max_parts >= (1ll << 31)) return false;
-  return encode_fn() != nullptr;
+  return tmap_available();
 }
 
 int launch_paged_decode_tc(const AttnParams& p, int q_dtype, cudaStream_t stream) {

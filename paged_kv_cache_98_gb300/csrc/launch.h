@@ -1,6 +1,7 @@
 // Internal launch interface between the C-ABI layer (api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -57,6 +58,17 @@ int launch_simt_bf16_e4m3(const AttnParams& p, int head_dim, int g_pad, cudaStre
 // KV head, 512-token partitions, decode rows only).
 bool tc_decode_supported(const AttnParams& p, int q_dtype, int kv_dtype, int head_dim);
 int launch_paged_decode_tc(const AttnParams& p, int q_dtype, cudaStream_t stream);
+
+// tcgen05 chunked-prefill attention (head_dim 128, 16-bit caches, 128 % g == 0).
+bool tc_prefill_supported(const AttnParams& p, int q_dtype, int kv_dtype, int head_dim);
+int launch_prefill_tc(const AttnParams& p, int q_dtype, int total_q, cudaStream_t stream);
+
+// Host helpers (host_util.cu).
+bool tmap_available();
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, bool bf16, uint32_t box_rows);
+bool make_map_q3d(CUtensorMap* m, const void* base, uint64_t tokens, uint32_t heads, bool bf16,
+                  uint32_t box_heads, uint32_t box_tokens);
+int sm_count();
 
 int launch_lse_merge(const AttnParams& p, int q_dtype, int head_dim, cudaStream_t stream);
 
