@@ -90,7 +90,7 @@ int run_attention(pkv::AttnParams& p, int q_dtype, int kv_dtype, int head_dim, f
   const int g_pad = pow2_at_least(p.group);
   int rc;
   if (pkv::tc_decode_supported(p, q_dtype, kv_dtype, head_dim))
-    rc = pkv::launch_paged_decode_tc(p, q_dtype, stream);
+    rc = pkv::launch_paged_decode_tc(p, q_dtype, kv_dtype, stream);
   else
     rc = pkv::launch_paged_attention_simt(p, q_dtype, kv_dtype, head_dim, g_pad, stream);
   if (rc != PKV_OK) return rc;

@@ -167,6 +167,12 @@ __device__ __forceinline__ void flag_error(uint32_t* errors, uint32_t bits) {
   if (errors) atomicOr(errors, bits);
 }
 
-__device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
+// 2^x with the hardware approximation (relative error about 2^-22; inputs
+// below -126 give 0).  Softmax weights are rounded to 16 bits afterwards.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 }  // namespace pkv

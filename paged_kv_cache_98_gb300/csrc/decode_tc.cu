@@ -29,6 +29,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstddef>
 #include <mutex>
 #include <type_traits>
 
@@ -39,7 +40,9 @@
 namespace pkv {
 namespace {
 
-constexpr int kTcThreads = 224;
+// warps 0-3 softmax/epilogue, 4 producer, 5 MMA, then 6 the V-tail fixer
+// (16-bit caches) or 6-9 the E4M3 -> fp16 converters (E4M3 caches)
+constexpr int tc_threads(bool fp8) { return fp8 ? 320 : 224; }
 constexpr int kTileKeys = 128;
 constexpr int kPart = 512;
 constexpr int kTilesPerPart = kPart / kTileKeys;
@@ -54,29 +57,44 @@ constexpr int kMaxSeqs = 1024;                    // sequences per launch (host 
 // The MMA always has N = 16; with at most 8 heads, Q and P keep 8 rows and the
 // descriptors' 8-row group stride is 0, so rows 8-15 alias rows 0-7 (their
 // products are never read).  The shared memory saved buys a sixth ring stage.
-template <bool G16>
+// E4M3 caches: TMA brings raw 16 KB tiles into a deep ring.  K tiles are
+// turned into fp16 by converter warps (E4M3 -> fp16 is exact) for the score
+// MMA; V tiles feed the P V product directly as 8-bit operands
+// (kind::f8f6f4), with P rounded to E4M3 after scaling by 2^8.  That keeps the
+// shared-memory traffic near four bytes per byte read from HBM.
+template <bool G16, bool FP8>
 struct Layout {
-  static constexpr int kStages = G16 ? 5 : 6;
+  static constexpr int kStages = FP8 ? 2 : (G16 ? 5 : 6);        // 16-bit tiles (E4M3: K only)
+  static constexpr int kRawStages = FP8 ? 8 : 1;                 // E4M3 tiles (K and V)
+  static constexpr int kRawBytes = FP8 ? kTileKeys * kD : 16;
   static constexpr int kRows = G16 ? 16 : 8;               // Q / P rows held
   static constexpr int kQHalf = kRows * 128;               // one 64-dim half of Q
   static constexpr int kQBytes = 2 * kQHalf;
   static constexpr int kQSbo = G16 ? 1024 : 0;
-  static constexpr int kPBytes = kRows * kPart * 2;
-  static constexpr int kPSbo = G16 ? kPGroupStride : 0;
+  // P: 16-bit, or E4M3 (1 byte) on E4M3 caches; 8-head groups in the N direction
+  static constexpr int kPElem = FP8 ? 1 : 2;
+  static constexpr int kPBytes = kRows * kPart * kPElem;
+  static constexpr int kPSbo = G16 ? (kPart / (16 / kPElem)) * 128 : 0;
 };
 
-template <bool G16>
+template <bool G16, bool FP8>
 struct Smem {
-  static constexpr int kStages = Layout<G16>::kStages;
-  uint8_t ring[kStages][kStageBytes];
-  uint8_t q[2][Layout<G16>::kQBytes];
-  uint8_t pmat[2][Layout<G16>::kPBytes];
-  float stat_m[2][16];
-  float stat_l[2][16];
+  using L = Layout<G16, FP8>;
+  static constexpr int kStages = L::kStages;
+  // every TMA destination / MMA operand sits on a 1024-byte boundary (the
+  // 128-byte swizzle repeats every 8 rows of 128 bytes)
+  alignas(1024) uint8_t ring[kStages][kStageBytes];
+  alignas(1024) uint8_t raw[L::kRawStages][L::kRawBytes];
+  alignas(1024) uint8_t q[2][L::kQBytes];
+  alignas(1024) uint8_t pmat[2][L::kPBytes];
+  float stat_inv[2][16];  // v_scale / l per head
+  float stat_lse[2][16];  // m + log2(l) per head
   float red_max[4][16];
   float red_sum[4][16];
   uint64_t full[kStages];
   uint64_t empty[kStages];
+  uint64_t raw_full[L::kRawStages];
+  uint64_t raw_empty[L::kRawStages];
   uint64_t q_full[2];
   uint64_t q_empty[2];
   uint64_t s_ready[2];
@@ -86,7 +104,7 @@ struct Smem {
   uint64_t mma_done;
   int seq_keys[kMaxSeqs];       // clamped context length of each sequence
   int seq_start[kMaxSeqs + 1];  // prefix sum of partitions per sequence
-  int scan[kTcThreads / 32];
+  int scan[10];  // per-warp partial sums (up to 10 warps)
   uint32_t tmem_base;
   int abort;
   uint32_t issued;  // ring positions the producer has issued so far
@@ -139,35 +157,63 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
-// All 128 softmax threads agree on `ok` (named barrier 1).
-__device__ __forceinline__ bool all_softmax(bool ok) {
+// All 128 threads of a group agree on `ok` (named barrier `id`).
+template <int id>
+__device__ __forceinline__ bool all_of_group(bool ok) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "bar.red.and.pred q, %2, 128, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"((uint32_t)ok)
+      : "r"((uint32_t)ok), "n"(id)
       : "memory");
   return r != 0;
 }
+__device__ __forceinline__ bool all_softmax(bool ok) { return all_of_group<1>(ok); }
 
-template <class QT, bool G16>
-__global__ void __launch_bounds__(kTcThreads, 1)
+// 16 E4M3 values -> 16 fp16 values equal to value * 2^-8, exactly, as two
+// 16-byte words.  Placing an E4M3 code's exponent and mantissa bits (e, m) at
+// fp16 bits 10..13 and 7..9 gives 2^(e-15)(1 + m/8) for e > 0 and
+// 2^-14 (m/8) for e = 0, i.e. the E4M3 value 2^(e-7)(1 + m/8) or 2^-6 (m/8)
+// times 2^-8; the sign bit moves from bit 7 to bit 15.  (The NaN codes
+// 0x7f / 0xff read as +-480 here; the cache write never produces them from
+// finite inputs.)  The 2^8 is folded into the softmax and output scales.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t w) {
+  return (w & 0x80008000u) | ((w >> 1) & 0x3F803F80u);
+}
+__device__ __forceinline__ void e4m3x16_to_f16(const uint4& v, uint4& lo, uint4& hi) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o[2 * i] = e4m3x2_to_f16x2_scaled(__byte_perm(u[i], 0u, 0x1404));      // bytes 0, 1
+    o[2 * i + 1] = e4m3x2_to_f16x2_scaled(__byte_perm(u[i], 0u, 0x3424));  // bytes 2, 3
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+template <class QT, bool G16, bool FP8>
+__global__ void __launch_bounds__(tc_threads(FP8), 1)
     paged_decode_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
                            const __grid_constant__ CUtensorMap tm_q, int kv_rows) {
   extern __shared__ uint8_t smem_raw[];
-  using L = Layout<G16>;
+  using L = Layout<G16, FP8>;
   constexpr int kStages = L::kStages;
+  constexpr int kRaw = L::kRawStages;
   constexpr int kQBytes = L::kQBytes;
   constexpr int kPBytes = L::kPBytes;
-  Smem<G16>& sm = *reinterpret_cast<Smem<G16>*>(
+  constexpr int kTcThreads = tc_threads(FP8);
+  // operands of the MMAs: fp16 when the cache is E4M3 (converted), else q's type
+  using PT = typename std::conditional<FP8, F16, QT>::type;
+  Smem<G16, FP8>& sm = *reinterpret_cast<Smem<G16, FP8>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool split = p.max_parts > 1;
-  constexpr uint32_t kAB = std::is_same<QT, BF16>::value ? 1u : 0u;
+  constexpr uint32_t kAB = std::is_same<PT, BF16>::value ? 1u : 0u;
   constexpr uint32_t kIdescS = tc::idesc_f16(kAB, 0, 0, 128, 16);
   constexpr uint32_t kIdescO = tc::idesc_f16(kAB, 1, 0, 128, 16);
 
@@ -176,6 +222,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
+    }
+    for (int s = 0; s < kRaw; ++s) {
+      mbar_init(&sm.raw_full[s], 1);
+      mbar_init(&sm.raw_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.q_full[b], 1);
@@ -257,6 +307,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int it = 0;
     bool ok = true;
     auto load_q = [&](const Item& x, int k) -> bool {
+      if constexpr (FP8) return true;  // the converter warps build fp16 Q
       const int b = k & 1;
       bool good = true;
       if (lane == 0) {
@@ -286,6 +337,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       return row;
     };
     auto load_tiles = [&](const Item& x, int row, const CUtensorMap* map) -> bool {
+      if constexpr (FP8) {
+        // raw E4M3 tiles: one 16-row box of 128 bytes per block
+        for (int t = 0; t < x.ntiles; ++t, ++pos) {
+          const int st = pos % kRaw;
+          bool good = true;
+          if (lane == 0) {
+            if (pos >= kRaw) good = wait_bar(&sm.raw_empty[st], ((pos / kRaw) - 1) & 1, abort);
+            if (good) mbar_arrive_expect_tx(&sm.raw_full[st], kTileKeys * kD);
+          }
+          if (!__shfl_sync(kFull, (int)good, 0)) return false;
+          if ((lane >> 3) == t)
+            tc::tma_load_2d(&sm.raw[st][0] + (lane & 7) * (kBlockSize * 128), map, 0, row,
+                            &sm.raw_full[st]);
+          __syncwarp();
+          if (lane == 0) *reinterpret_cast<volatile uint32_t*>(&sm.issued) = pos + 1;
+        }
+        return true;
+      }
       for (int t = 0; t < x.ntiles; ++t, ++pos) {
         const int st = pos % kStages;
         bool good = true;
@@ -327,14 +396,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (!ok && lane == 0) {
       flag_error(p.errors, PKV_DEVERR_TIMEOUT);
       // let copies already issued land before the CTA goes away
-      for (uint32_t x = pos > kStages ? pos - kStages : 0; x < pos; ++x)
-        mbar_wait(&sm.full[x % kStages], (x / kStages) & 1, 10000000ull);
+      if constexpr (FP8) {
+        for (uint32_t x = pos > kRaw ? pos - kRaw : 0; x < pos; ++x)
+          mbar_wait(&sm.raw_full[x % kRaw], (x / kRaw) & 1, 10000000ull);
+      } else {
+        for (uint32_t x = pos > kStages ? pos - kStages : 0; x < pos; ++x)
+          mbar_wait(&sm.full[x % kStages], (x / kStages) & 1, 10000000ull);
+      }
     }
   } else if (warp == 5) {
     // ---- MMA issuer ---------------------------------------------------------------------
     if (lane == 0) {
       int idx = blockIdx.x;
-      uint32_t pos = 0;
+      uint32_t pos = 0;   // position in the producer's ring
+      uint32_t kpos = 0;  // E4M3: position in the converted-K ring
       Item cur, nxt;
       int it = 0;
       bool ok = true;
@@ -343,8 +418,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!wait_bar(&sm.q_full[b], (k >> 1) & 1, abort)) return false;
         const uint32_t qa = smem_u32(&sm.q[b][0]);
         for (int t = 0; t < x.ntiles; ++t, ++pos) {
-          const int st = pos % kStages;
-          if (!wait_bar(&sm.full[st], (pos / kStages) & 1, abort)) return false;
+          const uint32_t rp = FP8 ? kpos++ : pos;
+          const int st = rp % kStages;
+          if (!wait_bar(&sm.full[st], (rp / kStages) & 1, abort)) return false;
           tc::fence_after_sync();
           const uint32_t ka = smem_u32(&sm.ring[st][0]);
 #pragma unroll
@@ -368,6 +444,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!wait_bar(&sm.v_fixed[b], (k >> 1) & 1, abort)) return false;
         tc::fence_after_sync();
         const uint32_t pa = smem_u32(&sm.pmat[b][0]);
+        if constexpr (FP8) {
+          // V^T (raw E4M3, MN-major: 128 dims = one swizzle atom wide) times
+          // P^T (E4M3, K-major), 32 keys per instruction
+          for (int t = 0; t < x.ntiles; ++t, ++pos) {
+            const int st = pos % kRaw;
+            if (!wait_bar(&sm.raw_full[st], (pos / kRaw) & 1, abort)) return false;
+            tc::fence_after_sync();
+            const uint32_t va = smem_u32(&sm.raw[st][0]);
+#pragma unroll
+            for (int kk = 0; kk < kTileKeys / 32; ++kk) {
+              const uint64_t a = tc::smem_desc(va + kk * (32 * 128), 16, 1024, tc::kLayoutSw128);
+              const uint64_t bp = tc::smem_desc(pa + (t * (kTileKeys / 16) + kk * 2) * 128, 128,
+                                                L::kPSbo, tc::kLayoutNone);
+              tc::mma_f8(tmem + b * 128 + 64, a, bp, kIdescO, (t | kk) != 0);
+            }
+            tc::mma_commit(&sm.raw_empty[st]);
+          }
+          tc::mma_commit(&sm.o_ready[b]);
+          return true;
+        }
         for (int t = 0; t < x.ntiles; ++t, ++pos) {
           const int st = pos % kStages;
           if (!wait_bar(&sm.full[st], (pos / kStages) & 1, abort)) return false;
@@ -401,7 +497,119 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::mma_commit(&sm.mma_done);
       mbar_wait(&sm.mma_done, 0, 100000000ull);
     }
-  } else if (warp == 6) {
+  } else if (FP8 && warp >= 6) {
+    // ---- E4M3 -> fp16 converters (warps 6-9) ---------------------------------------------
+    // Same item order as the producer: Q and K tiles of the next item, then V
+    // tiles of the current one.  Thread = tile row (key).  V rows at or past
+    // the partition's last key become zeros (0 * NaN would poison the MMA).
+    const int ctid = threadIdx.x - 192;
+    int idx = blockIdx.x;
+    uint32_t pos = 0;
+    Item cur, nxt;
+    int it = 0;
+    bool ok = true;
+    using QElem = typename QT::T;
+    auto conv_q = [&](const Item& x, int k) -> bool {
+      const int b = k & 1;
+      bool good = true;
+      if (k >= 2) good = wait_bar(&sm.q_empty[b], ((k - 2) >> 1) & 1, abort);
+      if (!all_of_group<2>(good)) return false;
+      for (int i = ctid; i < L::kRows * 16; i += 128) {
+        const int r = i >> 4, c = i & 15;
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (r < p.group) {
+          const QElem* src = static_cast<const QElem*>(p.q) +
+                             ((size_t)x.seq * p.num_heads + (size_t)x.kvh * p.group + r) * kD;
+          float f[8];
+          to_float(__ldg(reinterpret_cast<const uint4*>(src) + c), f, QT());
+          w = pack8(f, F16());
+        }
+        *reinterpret_cast<uint4*>(&sm.q[b][0] + (c >> 3) * L::kQHalf + r * 128 +
+                                  (((c & 7) ^ (r & 7)) * 16)) = w;
+      }
+      fence_proxy_async_smem();
+      tc::named_sync(2, 128);
+      if (ctid == 0) mbar_arrive(&sm.q_full[b]);
+      return true;
+    };
+    uint32_t kpos = 0;  // position in the converted-K ring
+    // Waits until the producer has issued ring position x: every earlier use
+    // of that stage is then complete, so a parity wait names this use.
+    auto wait_issued = [&](uint32_t x) -> bool {
+      const uint64_t t0 = globaltimer_ns();
+      while (*reinterpret_cast<volatile uint32_t*>(&sm.issued) <= x) {
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > 2000000000ull) {
+          *abort = 1;
+          return false;
+        }
+      }
+      return true;
+    };
+    auto conv_k = [&](const Item& x) -> bool {
+      for (int t = 0; t < x.ntiles; ++t, ++pos, ++kpos) {
+        const int rs = pos % kRaw, cs = kpos % kStages;
+        bool good = wait_issued(pos) && wait_bar(&sm.raw_full[rs], (pos / kRaw) & 1, abort);
+        if (good && kpos >= kStages)
+          good = wait_bar(&sm.empty[cs], ((kpos / kStages) - 1) & 1, abort);
+        if (!all_of_group<2>(good)) return false;
+        const int r = ctid;
+        const int sw = r & 7;
+        const uint8_t* src = &sm.raw[rs][0] + r * 128;
+        uint8_t* dst = &sm.ring[cs][0] + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // 16 E4M3 values = dims 16c .. 16c+15
+          uint4 lo, hi;
+          e4m3x16_to_f16(*reinterpret_cast<const uint4*>(src + ((c ^ sw) * 16)), lo, hi);
+          uint8_t* h = dst + (c >> 2) * kHalfBytes;
+          *reinterpret_cast<uint4*>(h + ((((2 * c) & 7) ^ sw) * 16)) = lo;
+          *reinterpret_cast<uint4*>(h + ((((2 * c + 1) & 7) ^ sw) * 16)) = hi;
+        }
+        fence_proxy_async_smem();
+        tc::named_sync(2, 128);
+        if (ctid == 0) {
+          mbar_arrive(&sm.full[cs]);
+          mbar_arrive(&sm.raw_empty[rs]);
+        }
+      }
+      return true;
+    };
+    // V tiles go to the MMA raw; rows at or past the partition's last key in a
+    // partial last block hold whatever the pool had there and become zeros
+    // (0 * NaN would poison the MMA).  At most one item ahead of the MMA.
+    auto fix_v = [&](const Item& x, int k) -> bool {
+      const int b = k & 1;
+      const uint32_t last = pos + x.ntiles - 1;
+      pos += x.ntiles;
+      bool good = true;
+      if (k >= 2) good = wait_bar(&sm.o_ready[b], ((k - 2) >> 1) & 1, abort);
+      const int tail = x.n & (kBlockSize - 1);
+      if (good && tail) good = wait_issued(last) && wait_bar(&sm.raw_full[last % kRaw], (last / kRaw) & 1, abort);
+      if (!all_of_group<2>(good)) return false;
+      if (tail) {
+        const int jb = ((x.n - 1) % kTileKeys) / kBlockSize;
+        const int rows = kBlockSize - tail;
+        uint8_t* base = &sm.raw[last % kRaw][0] + (jb * kBlockSize + tail) * 128;
+        for (int i = ctid; i < rows * 8; i += 128)
+          reinterpret_cast<uint4*>(base + (i >> 3) * 128)[i & 7] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+      }
+      tc::named_sync(2, 128);
+      if (ctid == 0) mbar_arrive(&sm.v_fixed[b]);
+      return true;
+    };
+    bool has = next_item(p, sm, idx, total, cur);
+    if (has) ok = conv_q(cur, 0) && conv_k(cur);
+    while (has && ok) {
+      const bool has_n = next_item(p, sm, idx, total, nxt);
+      if (has_n) ok = conv_q(nxt, it + 1) && conv_k(nxt);
+      if (ok) ok = fix_v(cur, it);
+      cur = nxt;
+      has = has_n;
+      ++it;
+    }
+    if (!ok && ctid == 0) flag_error(p.errors, PKV_DEVERR_TIMEOUT);
+  } else if (!FP8 && warp == 6) {
     // ---- V tail fixer -------------------------------------------------------------------
     // V rows past the context in a partial last block hold whatever the pool
     // had there; their P is zero, but 0 * NaN is NaN inside the MMA, so they
@@ -492,18 +700,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int d = tid;
       const int nparts = (x.keys + kPart - 1) / kPart;
       const bool direct = !split || nparts == 1;
+      const size_t head0 = (size_t)x.seq * p.num_heads + (size_t)x.kvh * p.group;
+      if (direct) {
+        OutT* dst = static_cast<OutT*>(p.out) + head0 * kD + d;
 #pragma unroll
-      for (int h = 0; h < L::kRows; ++h) {
-        if (h < p.group) {
-          const float val = o[h] * (p.v_scale / sm.stat_l[b][h]);
-          const size_t head = (size_t)x.seq * p.num_heads + (size_t)x.kvh * p.group + h;
-          if (direct) {
-            store_out(static_cast<OutT*>(p.out) + head * kD + d, val);
-          } else {
-            p.o_part[(head * p.max_parts + x.part) * kD + d] = val;
-            if (d == 0) p.lse[head * p.max_parts + x.part] = sm.stat_m[b][h] + log2f(sm.stat_l[b][h]);
-          }
-        }
+        for (int h = 0; h < L::kRows; ++h)
+          if (h < p.group) store_out(dst + h * kD, o[h] * sm.stat_inv[b][h]);
+      } else {
+        float* dst = p.o_part + (head0 * p.max_parts + x.part) * kD + d;
+        const size_t stride = (size_t)p.max_parts * kD;
+#pragma unroll
+        for (int h = 0; h < L::kRows; ++h)
+          if (h < p.group) dst[h * stride] = o[h] * sm.stat_inv[b][h];
+        if (d < p.group) p.lse[(head0 + d) * p.max_parts + x.part] = sm.stat_lse[b][d];
       }
       return true;
     };
@@ -559,13 +768,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int key = t * kTileKeys + tid;
           uint8_t* col = pm + (key >> 3) * 128 + (key & 7) * 2;
 #pragma unroll
-          for (int h = 0; h < L::kRows; ++h) {
+          for (int h = 0; h < L::kRows; h += 2) {
             if (h < p.group) {
-              const float e = fast_exp2(s[t][h] - mx[h]);
-              sum[h] += e;
-              OutT pv;
-              store_out(&pv, e);
-              *reinterpret_cast<OutT*>(col + (h >> 3) * kPGroupStride + (h & 7) * 16) = pv;
+              const float e0 = fast_exp2(s[t][h] - mx[h]);
+              const float e1 = h + 1 < p.group ? fast_exp2(s[t][h + 1] - mx[h + 1]) : 0.0f;
+              sum[h] += e0;
+              sum[h + 1] += e1;
+              if constexpr (FP8) {
+                // E4M3 with a 2^8 scale (weights are <= 1), core matrices of 16 keys
+                const __nv_fp8x2_storage_t q2 =
+                    __nv_cvt_float2_to_fp8x2(make_float2(e0 * 256.0f, e1 * 256.0f),
+                                             __NV_SATFINITE, __NV_E4M3);
+                uint8_t* c8 = pm + (key >> 4) * 128 + (h >> 3) * L::kPSbo + (h & 7) * 16 + (key & 15);
+                c8[0] = (uint8_t)(q2 & 0xffu);
+                if (h + 1 < p.group) c8[16] = (uint8_t)(q2 >> 8);
+                continue;
+              }
+              uint32_t pr;
+              if constexpr (std::is_same<PT, BF16>::value) {
+                __nv_bfloat162 v2 = __floats2bfloat162_rn(e0, e1);
+                pr = *reinterpret_cast<uint32_t*>(&v2);
+              } else {
+                __half2 v2 = __floats2half2_rn(e0, e1);
+                pr = *reinterpret_cast<uint32_t*>(&v2);
+              }
+              uint8_t* c0 = col + (h >> 3) * kPGroupStride + (h & 7) * 16;
+              *reinterpret_cast<uint16_t*>(c0) = (uint16_t)(pr & 0xffffu);
+              if (h + 1 < p.group) *reinterpret_cast<uint16_t*>(c0 + 16) = (uint16_t)(pr >> 16);
             }
           }
         }
@@ -584,10 +813,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (tid == 0) mbar_arrive(&sm.p_ready[b]);
       // read by this item's epilogue, after the next item's barriers
       if (tid < 16 && tid < p.group) {
-        sm.stat_m[b][tid] = fmaxf(fmaxf(sm.red_max[0][tid], sm.red_max[1][tid]),
-                                  fmaxf(sm.red_max[2][tid], sm.red_max[3][tid]));
-        sm.stat_l[b][tid] =
+        const float m = fmaxf(fmaxf(sm.red_max[0][tid], sm.red_max[1][tid]),
+                              fmaxf(sm.red_max[2][tid], sm.red_max[3][tid]));
+        const float l =
             (sm.red_sum[0][tid] + sm.red_sum[1][tid]) + (sm.red_sum[2][tid] + sm.red_sum[3][tid]);
+        sm.stat_inv[b][tid] = p.v_scale / (FP8 ? l * 256.0f : l);
+        sm.stat_lse[b][tid] = m + log2f(l);
       }
 
       if (have_prev) {
@@ -613,16 +844,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // ---- host side ---------------------------------------------------------------------------
-template <class QT, bool G16>
+template <class QT, bool G16, bool FP8>
 int launch_tc_typed(const AttnParams& p, cudaStream_t stream) {
   const bool bf16 = std::is_same<QT, BF16>::value;
   const uint64_t kv_rows = (uint64_t)p.num_blocks * p.num_kv_heads * kBlockSize;
   CUtensorMap tk, tv;
-  if (!make_map_2d(&tk, p.k_cache, kv_rows, bf16, 16) || !make_map_2d(&tv, p.v_cache, kv_rows, bf16, 16))
-    return PKV_ERR_CUDA;
-  const size_t smem = sizeof(Smem<G16>) + 1024;
-  static_assert(sizeof(Smem<G16>) + 1024 <= 232448, "shared memory budget of one CTA");
-  auto kern = paged_decode_tc_kernel<QT, G16>;
+  const bool maps = FP8 ? make_map_e4m3(&tk, p.k_cache, kv_rows, 16) &&
+                              make_map_e4m3(&tv, p.v_cache, kv_rows, 16)
+                        : make_map_2d(&tk, p.k_cache, kv_rows, bf16, 16) &&
+                              make_map_2d(&tv, p.v_cache, kv_rows, bf16, 16);
+  if (!maps) return PKV_ERR_CUDA;
+  using SM = Smem<G16, FP8>;
+  const size_t smem = sizeof(SM) + 1024;
+  static_assert(sizeof(SM) + 1024 <= 232448, "shared memory budget of one CTA");
+  static_assert(offsetof(SM, ring) % 1024 == 0 && offsetof(SM, raw) % 1024 == 0 &&
+                    offsetof(SM, q) % 1024 == 0 && offsetof(SM, pmat) % 1024 == 0 &&
+                    kStageBytes % 1024 == 0 && Layout<G16, FP8>::kQHalf % 1024 == 0,
+                "swizzled buffers must start on 1024-byte boundaries");
+  auto kern = paged_decode_tc_kernel<QT, G16, FP8>;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -634,6 +873,7 @@ int launch_tc_typed(const AttnParams& p, cudaStream_t stream) {
   // launches of at most kMaxSeqs sequences each (their rows are independent)
   for (int r0 = 0; r0 < p.num_rows; r0 += kMaxSeqs) {
     AttnParams c = p;
+    if (FP8) c.q_scale *= 256.0f;  // the converted K tiles hold value * 2^-8
     c.num_rows = p.num_rows - r0 < kMaxSeqs ? p.num_rows - r0 : kMaxSeqs;
     c.num_seqs = c.num_rows;
     const size_t head0 = (size_t)r0 * p.num_heads;
@@ -645,14 +885,15 @@ int launch_tc_typed(const AttnParams& p, cudaStream_t stream) {
       c.lse = p.lse + head0 * p.max_parts;
       c.o_part = p.o_part + head0 * p.max_parts * kD;
     }
-    CUtensorMap tq;
-    if (!make_map_2d(&tq, c.q, (uint64_t)c.num_rows * p.num_heads, bf16, Layout<G16>::kRows))
+    CUtensorMap tq;  // read by TMA on 16-bit caches, unused (converted Q) on E4M3
+    if (!make_map_2d(&tq, c.q, (uint64_t)c.num_rows * p.num_heads, bf16,
+                     Layout<G16, FP8>::kRows))
       return PKV_ERR_CUDA;
     const long long items = (long long)c.num_rows * p.num_kv_heads * p.max_parts;
     int grid = sm_count();
     if (items < grid) grid = (int)items;
     if (grid < 1) grid = 1;
-    kern<<<grid, kTcThreads, smem, stream>>>(c, tk, tv, tq, (int)kv_rows);
+    kern<<<grid, tc_threads(FP8), smem, stream>>>(c, tk, tv, tq, (int)kv_rows);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   }
   return PKV_OK;
@@ -661,7 +902,7 @@ int launch_tc_typed(const AttnParams& p, cudaStream_t stream) {
 }  // namespace
 
 bool tc_decode_supported(const AttnParams& p, int q_dtype, int kv_dtype, int head_dim) {
-  if (head_dim != kD || kv_dtype != q_dtype) return false;
+  if (head_dim != kD || (kv_dtype != q_dtype && kv_dtype != PKV_FP8_E4M3)) return false;
   if (p.query_start_loc != nullptr || p.partition != kPart) return false;
   if (p.group < 2 || p.group > 16) return false;
   const uint64_t kv_rows = (uint64_t)p.num_blocks * p.num_kv_heads * kBlockSize;
@@ -671,11 +912,20 @@ bool tc_decode_supported(const AttnParams& p, int q_dtype, int kv_dtype, int hea
   return tmap_available();
 }
 
-int launch_paged_decode_tc(const AttnParams& p, int q_dtype, cudaStream_t stream) {
+int launch_paged_decode_tc(const AttnParams& p, int q_dtype, int kv_dtype, cudaStream_t stream) {
   const bool g16 = p.group > 8;
+  if (kv_dtype == PKV_FP8_E4M3) {
+    if (q_dtype == PKV_BF16)
+      return g16 ? launch_tc_typed<BF16, true, true>(p, stream)
+                 : launch_tc_typed<BF16, false, true>(p, stream);
+    return g16 ? launch_tc_typed<F16, true, true>(p, stream)
+               : launch_tc_typed<F16, false, true>(p, stream);
+  }
   if (q_dtype == PKV_BF16)
-    return g16 ? launch_tc_typed<BF16, true>(p, stream) : launch_tc_typed<BF16, false>(p, stream);
-  return g16 ? launch_tc_typed<F16, true>(p, stream) : launch_tc_typed<F16, false>(p, stream);
+    return g16 ? launch_tc_typed<BF16, true, false>(p, stream)
+               : launch_tc_typed<BF16, false, false>(p, stream);
+  return g16 ? launch_tc_typed<F16, true, false>(p, stream)
+             : launch_tc_typed<F16, false, false>(p, stream);
 }
 
 }  // namespace pkv

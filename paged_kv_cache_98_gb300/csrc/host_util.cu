@@ -45,6 +45,19 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, bool bf16, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Rows of 128 one-byte E4M3 values; boxes of 128 columns x box_rows rows; 128-byte swizzle.
+bool make_map_e4m3(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // q viewed as [tokens][heads][128]: boxes of 64 columns x box_heads heads x
 // box_tokens tokens, 128-byte swizzle (the box lands as box_heads*box_tokens
 // rows of 128 bytes, token-major).

@@ -54,10 +54,10 @@ int launch_simt_f16_e4m3(const AttnParams& p, int head_dim, int g_pad, cudaStrea
 int launch_simt_bf16_bf16(const AttnParams& p, int head_dim, int g_pad, cudaStream_t s);
 int launch_simt_bf16_e4m3(const AttnParams& p, int head_dim, int g_pad, cudaStream_t s);
 
-// tcgen05 grouped-query decode (head_dim 128, 16-bit caches, 2..16 heads per
-// KV head, 512-token partitions, decode rows only).
+// tcgen05 grouped-query decode (head_dim 128, 16-bit or E4M3 caches, 2..16
+// heads per KV head, 512-token partitions, decode rows only).
 bool tc_decode_supported(const AttnParams& p, int q_dtype, int kv_dtype, int head_dim);
-int launch_paged_decode_tc(const AttnParams& p, int q_dtype, cudaStream_t stream);
+int launch_paged_decode_tc(const AttnParams& p, int q_dtype, int kv_dtype, cudaStream_t stream);
 
 // tcgen05 chunked-prefill attention (head_dim 128, 16-bit caches, 128 % g == 0).
 bool tc_prefill_supported(const AttnParams& p, int q_dtype, int kv_dtype, int head_dim);
@@ -68,6 +68,7 @@ bool tmap_available();
 bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, bool bf16, uint32_t box_rows);
 bool make_map_q3d(CUtensorMap* m, const void* base, uint64_t tokens, uint32_t heads, bool bf16,
                   uint32_t box_heads, uint32_t box_tokens);
+bool make_map_e4m3(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows);
 int sm_count();
 
 int launch_lse_merge(const AttnParams& p, int q_dtype, int head_dim, cudaStream_t stream);

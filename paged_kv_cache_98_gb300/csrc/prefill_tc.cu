@@ -24,6 +24,7 @@
 
 #include <cuda.h>
 
+#include <cstddef>
 #include <type_traits>
 
 #include "common.cuh"
@@ -45,9 +46,9 @@ constexpr int kTmemCols = 512;  // S (2 x 128) + O (128), rounded up
 constexpr float kRescaleAt = 8.0f;
 
 struct Smem {
-  uint8_t ring[kStages][kTileBytes];
-  uint8_t q[kTileBytes];
-  uint8_t pmat[2][kTileBytes];
+  alignas(1024) uint8_t ring[kStages][kTileBytes];
+  alignas(1024) uint8_t q[kTileBytes];
+  alignas(1024) uint8_t pmat[2][kTileBytes];
   int seq_start[kMaxSeqs + 1];  // prefix of query-row tiles per sequence
   int seq_qlen[kMaxSeqs];
   int seq_ctx[kMaxSeqs];
@@ -252,14 +253,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return row;
     };
-    int ck = -1, cv = -1, rk = kv_rows, rv = kv_rows;
+    // Block rows of K chunk ck (current), ck-1 (still needed by the V tiles,
+    // which lag one tile) and ck+1 (loaded one chunk ahead so its latency hides).
+    int ck = 0, r_prev = kv_rows, r_cur = kv_rows, r_next = kv_rows;
     auto issue = [&](int t, bool is_v) -> bool {
       const int c = t >> 2;
-      if (is_v) {
-        if (c != cv) { rv = rows_for(c); cv = c; }
-      } else {
-        if (c != ck) { rk = rows_for(c); ck = c; }
+      if (!is_v && c != ck) {  // K moves to the next chunk
+        r_prev = r_cur;
+        r_cur = r_next;
+        r_next = rows_for(c + 1);
+        ck = c;
       }
+      const int row = (is_v && c != ck) ? r_prev : r_cur;
       const int st = pos % kStages;
       bool good = true;
       if (lane == 0) {
@@ -270,7 +275,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if ((lane >> 3) == (t & 3)) {
         uint8_t* dst = &sm.ring[st][0] + (lane & 7) * (kBlockSize * 128);
         const CUtensorMap* map = is_v ? &tm_v : &tm_k;
-        const int row = is_v ? rv : rk;
         tc::tma_load_2d(dst, map, 0, row, &sm.full[st]);
         tc::tma_load_2d(dst + kHalf, map, 64, row, &sm.full[st]);
       }
@@ -280,7 +284,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     while (ok && next_item(p, sm, idx, total, x)) {
-      ck = cv = -1;
+      ck = 0;
+      r_prev = kv_rows;
+      r_cur = rows_for(0);
+      r_next = rows_for(1);
       bool good = true;
       if (lane == 0) {
         if (nitem >= 1) good = wait_bar(&sm.q_empty, (nitem - 1) & 1, abort);
@@ -542,6 +549,9 @@ int launch_typed(const AttnParams& p, int total_q, cudaStream_t stream) {
     return PKV_ERR_CUDA;
   const size_t smem = sizeof(Smem) + 1024;
   static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory budget of one CTA");
+  static_assert(offsetof(Smem, ring) % 1024 == 0 && offsetof(Smem, q) % 1024 == 0 &&
+                    offsetof(Smem, pmat) % 1024 == 0,
+                "swizzled buffers must start on 1024-byte boundaries");
   auto kern = prefill_tc_kernel<QT>;
   static bool configured = false;
   if (!configured) {

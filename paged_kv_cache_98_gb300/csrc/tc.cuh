@@ -104,8 +104,9 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)layout << 61);
 }
 
-// Instruction descriptor of kind::f16 with fp32 accumulation.
-// ab: 0 = f16 operands, 1 = bf16 operands.  a_mn / b_mn: operand stored
+// Instruction descriptor with fp32 accumulation (same layout for kind::f16
+// and kind::f8f6f4).  ab: operand format code; kind::f16: 0 = f16, 1 = bf16;
+// kind::f8f6f4: 0 = E4M3.  a_mn / b_mn: operand stored
 // MN-major (1) or K-major (0).
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab, uint32_t a_mn, uint32_t b_mn,
                                                  uint32_t M, uint32_t N) {
@@ -120,6 +121,18 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T with 8-bit operands (kind::f8f6f4,
+// K = 32 per instruction), issued by one thread.
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                      uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }

@@ -278,6 +278,12 @@ def llama2_7b_x16(seed: int = 1) -> Workload:
     return llama2_7b(seed, num_seqs=16)
 
 
+def long_fp8_x2(seed: int = 4) -> Workload:
+    """The long-context FP8 shape with 2 sequences (0.54 GB of K/V): a smaller
+    case of the same kernel for detailed profiling."""
+    return long_fp8(seed, num_seqs=2)
+
+
 NAMED = {
     "tiny": tiny,
     "llama2_7b": llama2_7b,
@@ -285,6 +291,7 @@ NAMED = {
     "gqa70b_shared": gqa70b_shared,
     "mixed": mixed,
     "long_fp8": long_fp8,
+    "long_fp8_x2": long_fp8_x2,
 }
 
 
