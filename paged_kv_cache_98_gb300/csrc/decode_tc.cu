@@ -32,8 +32,8 @@
 // accumulation) directly.  E4M3 scores: each query row is split as
 // q / s = hi + lo with hi, lo in E4M3 and s = max|q| / 448 (together about 8
 // significant bits, like bf16); hi rows and lo rows are the N columns of one
-// MMA and the softmax adds them.  E4M3 output: P is rounded to E4M3 after a
-// 2^8 scale.  Shared-memory traffic stays at two bytes per byte read from HBM.
+// MMA (fewer, wider MMAs issue faster) and the softmax adds them.  E4M3
+// output: P is rounded to E4M3 after a 2^8 scale.  Shared-memory traffic stays at two bytes per byte read from HBM.
 //
 // The last block of a context is usually partial: rows past the last key hold
 // whatever the pool had there.  Their weights are zero, but 0 * NaN is NaN
@@ -68,7 +68,7 @@ constexpr int kTailBytes = 4096;                  // one MMA K step of V rows
 
 // With at most 8 heads (G16 false) the 16-bit Q and P keep 8 rows and the
 // descriptors' 8-row group stride is 0 (rows 8-15 alias rows 0-7; their
-// products are never read); the E4M3 Q holds 8 hi + 8 lo rows.
+// products are never read); the E4M3 Q holds the hi rows, then the lo rows.
 template <bool G16, bool FP8>
 struct Layout {
   static constexpr int kTileBytes = FP8 ? kTileKeys * kD : kTileKeys * kD * 2;
@@ -708,7 +708,6 @@ __global__ void __launch_bounds__(tc_threads(FP8), 1)
       ok = all_softmax(wait_bar(&sm.s_ready[b], (it >> 1) & 1, abort));
       if (!ok) break;
       tc::fence_after_sync();
-      float s[kTilesPerPart][16];
       float qsh[16];  // scale of each head's scores (base 2)
       if constexpr (FP8) {
         // per-row scales of the split query: published by the converters
@@ -716,16 +715,19 @@ __global__ void __launch_bounds__(tc_threads(FP8), 1)
         if (!ok) break;
 #pragma unroll
         for (int h = 0; h < L::kRows; ++h) qsh[h] = qs * sm.qscale[it & 3][h];
+      }
+      float s[kTilesPerPart][16];
+      if constexpr (FP8 && G16) {
+        // 32 columns (16 hi, 16 lo) per tile: one tile at a time
 #pragma unroll
         for (int t = 0; t < kTilesPerPart; ++t) {
           if (t < cur.ntiles) {
-            float hl[L::kQRows];
-#pragma unroll
-            for (int c = 0; c < L::kQRows; c += 16)
-              tc::tmem_ld16(tmem + lane_off + b * L::kBufCols + t * L::kSCols + c, hl + c);
+            float hl[32];
+            tc::tmem_ld16(tmem + lane_off + b * L::kBufCols + t * L::kSCols, hl);
+            tc::tmem_ld16(tmem + lane_off + b * L::kBufCols + t * L::kSCols + 16, hl + 16);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int h = 0; h < L::kRows; ++h) s[t][h] = hl[h] + hl[h + L::kRows];
+            for (int h = 0; h < 16; ++h) s[t][h] = hl[h] + hl[h + 16];
           }
         }
       } else {
@@ -734,6 +736,13 @@ __global__ void __launch_bounds__(tc_threads(FP8), 1)
           if (t < cur.ntiles)
             tc::tmem_ld16(tmem + lane_off + b * L::kBufCols + t * L::kSCols, s[t]);
         tc::tmem_wait_ld();
+        if constexpr (FP8) {
+          // columns 0-7 hi, 8-15 lo
+#pragma unroll
+          for (int t = 0; t < kTilesPerPart; ++t)
+#pragma unroll
+            for (int h = 0; h < 8; ++h) s[t][h] += s[t][h + 8];
+        }
       }
       // running max per head over this thread's keys, then over the CTA
       float mx[16];
