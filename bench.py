@@ -55,6 +55,15 @@ def parse_args():
 
 
 # ---- environment -----------------------------------------------------------------
+# ncu summaries under profiles/ whose recorded DRAM traffic belongs to the decode
+# kernel of each workload (other workloads report no traffic)
+TRAFFIC_PROFILES = {
+    "llama2_7b": "decode_llama2_7b",
+    "gqa70b_shared": "decode_gqa70b_shared_tc",
+    "long_fp8": "decode_long_fp8_tc",
+}
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -476,7 +485,7 @@ def main():
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
             "peak_kind": f"{peak_kind} HBM copy bandwidth",
             "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "traffic": recorded_traffic("decode_llama2_7b"),
+            "traffic": recorded_traffic(TRAFFIC_PROFILES.get(args.workload, "")),
             "algorithmic_bytes_per_launch": kv_bytes,
             "decode_ms": round(dec_ms, 5), "write_ms": round(res["write_ms"], 5),
         },

@@ -7,23 +7,30 @@
 // devpress.csdn.net vLLM overview, "9、FlashAttention (3)/(4)" (query blocks
 // against streamed key/value blocks, running max and sum of exponentials).
 //
-// Work item = (sequence, KV head, tile of 128 query rows), a row being a
-// (query token, head of the group) pair, token-major, so that the g heads of a
-// KV head share every K/V tile.  Per 128-key tile j of the visible context:
-//   S_j = Q K_j^T              tcgen05, M = 128 rows, N = 128 keys, fp32 in TMEM
-//   online softmax per row     four warps, thread = row = TMEM lane; causal mask
-//   O  += P_j V_j              tcgen05, A = P (bf16/fp16 in shared memory), B = V
-// The running max is only moved (and O rescaled in TMEM) when a row's tile max
-// exceeds it by more than 8 in base-2 units, so exponentials stay <= 2^8 and
-// most tiles need no rescale; the final division by the row sum is exact.
-// The MMA issuer runs S one tile ahead of the P V product (S double-buffered
-// in TMEM), so the softmax of tile j overlaps the MMAs of tile j+1.
+// A query tile is 128 rows, a row being a (query token, head of the group)
+// pair, token-major, so that the g heads of a KV head share every K/V tile.
+// Work item = (sequence, KV head, two consecutive query tiles a and b): each
+// K/V tile brought into shared memory feeds both.  Per 128-key tile j:
+//   S_x = Q_x K_j^T     tcgen05, M = 128 rows, N = 128 keys, fp32 in TMEM
+//   softmax of tile x   warpgroup x (thread = row = TMEM lane): scores -> P,
+//                       written back over S_x in TMEM as packed 16-bit pairs
+//   O_x += P_x V_j      tcgen05 with A = P_x read from TMEM, B = V_j
+// for x = a, b.  The two softmax warpgroups alternate with the MMAs: while
+// warpgroup a turns S_a into P_a, the tensor pipe computes S_b, and the other
+// way round.  The running max only moves (and O is rescaled in TMEM) when a
+// row's tile max exceeds it by more than 8 in base-2 units; the final
+// division by the row sum is exact.
 //
-// Warps: 0-3 softmax + epilogue, 4 TMA producer (Q with one 3-D box per half,
-// K/V with one 16-row box per block and half), 5 TMEM owner + MMA issuer.
+// Warps: 0-3 softmax + epilogue of tile a, 4-7 of tile b, 8 TMEM owner + MMA
+// issuer, 9-11 TMA producers.  A K/V tile is 16 boxes of 16 rows x 128 B (one
+// per block and half); the boxes of each tile are spread over the three
+// producer warps, since one warp issuing boxes of this size moves about 31
+// GB/s per SM and three about 40.  Producer 0 also loads Q (one 3-D box per
+// half) and the partial last block of V.
 
 #include <cuda.h>
 
+#include <climits>
 #include <cstddef>
 #include <type_traits>
 
@@ -34,22 +41,26 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
+constexpr int kProducers = 3;  // warps 9..11
 constexpr int kD = 128;
 constexpr int kTileKeys = 128;
 constexpr int kRowsM = 128;
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kTileBytes = 128 * kD * 2;  // 32 KB: [2 halves][128 rows][128 B]
 constexpr int kHalf = kTileBytes / 2;
+constexpr int kTailBytes = kBlockSize * kD * 2;  // one block of V: [2 halves][16 rows][128 B]
 constexpr int kMaxSeqs = 1024;
-constexpr int kTmemCols = 512;  // S (2 x 128) + O (128), rounded up
+constexpr int kTmemCols = 512;  // S/P a, S/P b, O a, O b
+constexpr uint32_t kColO = 256;
 constexpr float kRescaleAt = 8.0f;
+constexpr int kBeyond = INT_MIN;  // block past the context (the box reads zeros)
 
 struct Smem {
   alignas(1024) uint8_t ring[kStages][kTileBytes];
-  alignas(1024) uint8_t q[kTileBytes];
-  alignas(1024) uint8_t pmat[2][kTileBytes];
-  int seq_start[kMaxSeqs + 1];  // prefix of query-row tiles per sequence
+  alignas(1024) uint8_t q[2][kTileBytes];
+  alignas(1024) uint8_t tail[kTailBytes];
+  int seq_start[kMaxSeqs + 1];  // prefix of tile pairs per sequence
   int seq_qlen[kMaxSeqs];
   int seq_ctx[kMaxSeqs];
   int seq_q0[kMaxSeqs];
@@ -58,18 +69,24 @@ struct Smem {
   uint64_t empty[kStages];
   uint64_t q_full;
   uint64_t q_empty;
-  uint64_t s_ready[2];
+  uint64_t s_ready[2];  // per query tile
   uint64_t p_ready[2];
   uint64_t o_done[2];
-  uint64_t o_free;
+  uint64_t o_free[2];
+  uint64_t tail_full;
+  uint64_t tail_free;
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
-  uint32_t issued;
 };
 
 struct Item {
-  int seq, kvh, t0, nt, qlen, ctx, q0, pos0, nkt;
+  int seq, kvh, ctx, q0;
+  int t0[2], nt[2];  // first token (within the chunk) and tokens of tiles a, b (nt[1] = 0: none)
+  int pos0[2];       // absolute position of each tile's first token
+  int nkt[2];        // key tiles each query tile attends
+  int nk;            // key tiles of the item (max of the two)
+  int tail_step;     // 16-key MMA step of the last key tile holding a partial block, else -1
 };
 
 __device__ __forceinline__ bool next_item(const AttnParams& p, const Smem& sm, int& idx,
@@ -84,18 +101,27 @@ __device__ __forceinline__ bool next_item(const AttnParams& p, const Smem& sm, i
     const int mid = (lo + hi + 1) >> 1;
     if (sm.seq_start[mid] <= pair) lo = mid; else hi = mid - 1;
   }
-  const int ntile = sm.seq_start[lo + 1] - sm.seq_start[lo];
-  const int mt = ntile - 1 - (pair - sm.seq_start[lo]);  // longest tiles first
-  const int rpt = kRowsM / p.group;                      // tokens per tile
+  const int npairs = sm.seq_start[lo + 1] - sm.seq_start[lo];
+  const int mp = npairs - 1 - (pair - sm.seq_start[lo]);  // longest pairs first
+  const int rpt = kRowsM / p.group;                        // tokens per tile
+  const int qlen = sm.seq_qlen[lo];
   it.seq = lo;
   it.kvh = kvh;
-  it.qlen = sm.seq_qlen[lo];
   it.ctx = sm.seq_ctx[lo];
   it.q0 = sm.seq_q0[lo];
-  it.t0 = mt * rpt;
-  it.nt = min(rpt, it.qlen - it.t0);
-  it.pos0 = it.ctx - it.qlen + it.t0;
-  it.nkt = (it.pos0 + it.nt - 1) / kTileKeys + 1;
+  it.nk = 0;
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    it.t0[x] = (2 * mp + x) * rpt;
+    it.nt[x] = max(0, min(rpt, qlen - it.t0[x]));
+    it.pos0[x] = it.ctx - qlen + it.t0[x];
+    it.nkt[x] = it.nt[x] > 0 ? (it.pos0[x] + it.nt[x] - 1) / kTileKeys + 1 : 0;
+    it.nk = max(it.nk, it.nkt[x]);
+  }
+  const bool partial = (it.ctx & (kBlockSize - 1)) != 0;
+  it.tail_step = partial && (it.ctx - 1) / kTileKeys == it.nk - 1
+                     ? ((it.ctx - 1) % kTileKeys) / kBlockSize
+                     : -1;
   return true;
 }
 
@@ -114,15 +140,16 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
-__device__ __forceinline__ bool all_softmax(bool ok) {
+// All 128 threads of softmax warpgroup x agree on `ok` (named barrier 1 + x).
+__device__ __forceinline__ bool all_group(bool ok, int x) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "bar.red.and.pred q, %2, 128, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"((uint32_t)ok)
+      : "r"((uint32_t)ok), "r"(1 + x)
       : "memory");
   return r != 0;
 }
@@ -136,6 +163,18 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&h);
   }
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, 16-bit operands: A is M lanes x K
+// elements, two elements per 32-bit column (the lower half holds the even one).
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 template <class QT>
@@ -155,34 +194,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- set-up ---------------------------------------------------------------------------
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.full[s], kProducers);
       mbar_init(&sm.empty[s], 1);
     }
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_empty, 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.s_ready[b], 1);
-      mbar_init(&sm.p_ready[b], 1);
-      mbar_init(&sm.o_done[b], 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&sm.s_ready[x], 1);
+      mbar_init(&sm.p_ready[x], 1);
+      mbar_init(&sm.o_done[x], 1);
+      mbar_init(&sm.o_free[x], 1);
     }
-    mbar_init(&sm.o_free, 1);
+    mbar_init(&sm.tail_full, 1);
+    mbar_init(&sm.tail_free, 1);
     mbar_init(&sm.mma_done, 1);
     sm.abort = 0;
-    sm.issued = 0;
     fence_barrier_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp >= 9 && lane == 0) {
     tc::prefetch_tmap(&tm_k);
     tc::prefetch_tmap(&tm_v);
     tc::prefetch_tmap(&tm_q);
   }
-  if (warp == 5) {
+  if (warp == 8) {
     tc::tmem_alloc(&sm.tmem_base, kTmemCols);
     tc::tmem_relinquish();
   }
   {
     // per-sequence query length, context, first query row, and the prefix
-    // of 128-row tiles
+    // of tile pairs
     const int S = p.num_seqs, tid = threadIdx.x;
     const int chunk = (S + kThreads - 1) / kThreads;
     const int cap = p.max_blocks_per_seq * kBlockSize;
@@ -202,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm.seq_qlen[sq] = qlen;
         sm.seq_ctx[sq] = ctx;
         sm.seq_q0[sq] = q0;
-        local += (qlen * g + kRowsM - 1) / kRowsM;
+        const int tiles = (qlen * g + kRowsM - 1) / kRowsM;
+        local += (tiles + 1) / 2;
       }
     }
     int incl = local;
@@ -220,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sq = tid * chunk + i;
       if (sq < S) {
         sm.seq_start[sq] = run;
-        run += (sm.seq_qlen[sq] * g + kRowsM - 1) / kRowsM;
+        run += ((sm.seq_qlen[sq] * g + kRowsM - 1) / kRowsM + 1) / 2;
       }
     }
     if (tid == kThreads - 1) sm.seq_start[S] = base + incl;
@@ -232,80 +273,102 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = &sm.abort;
   const int total = sm.seq_start[p.num_seqs] * p.num_kv_heads;
 
-  if (warp == 4) {
-    // ---- TMA producer ---------------------------------------------------------------------
+  if (warp >= 9) {
+    // ---- TMA producers (ring order K0, V0, K1, V1, ...) -----------------------------------
+    // Producer pw issues the boxes of blocks j with j % 3 == pw of every tile.
+    const int pw = warp - 9;
+    const int mine = (8 - pw + kProducers - 1) / kProducers;  // blocks per tile: 3, 3, 2
+    const bool my_lane = (lane & 7) % kProducers == pw;
     int idx = blockIdx.x;
     uint32_t pos = 0;
-    int nitem = 0;
+    int nitem = 0, ntail = 0;
     bool ok = true;
     Item x;
-    // lane j: cache row of block 32*c + j of the item's key range
-    auto rows_for = [&](int c) -> int {
+    // block id of block 32c + lane of the item's context (kBeyond past it);
+    // read ahead of its use, checked when used
+    auto fetch = [&](int c) -> int {
       const int b = 32 * c + lane;
-      const int nblk = (x.ctx + kBlockSize - 1) / kBlockSize;
-      int row = kv_rows;
-      if (b < nblk) {
-        const int blk = __ldg(p.block_tables + (size_t)x.seq * p.max_blocks_per_seq + b);
-        if (blk >= 0 && blk < p.num_blocks)
-          row = (blk * p.num_kv_heads + x.kvh) * kBlockSize;
-        else
-          flag_error(p.errors, PKV_DEVERR_BLOCK_ID);
-      }
-      return row;
+      return b < (x.ctx + kBlockSize - 1) / kBlockSize
+                 ? __ldg(p.block_tables + (size_t)x.seq * p.max_blocks_per_seq + b)
+                 : kBeyond;
     };
-    // Block rows of K chunk ck (current), ck-1 (still needed by the V tiles,
-    // which lag one tile) and ck+1 (loaded one chunk ahead so its latency hides).
-    int ck = 0, r_prev = kv_rows, r_cur = kv_rows, r_next = kv_rows;
-    auto issue = [&](int t, bool is_v) -> bool {
-      const int c = t >> 2;
-      if (!is_v && c != ck) {  // K moves to the next chunk
-        r_prev = r_cur;
-        r_cur = r_next;
-        r_next = rows_for(c + 1);
-        ck = c;
-      }
-      const int row = (is_v && c != ck) ? r_prev : r_cur;
+    auto to_row = [&](int blk) -> int {
+      if (blk == kBeyond) return kv_rows;
+      if (blk >= 0 && blk < p.num_blocks) return (blk * p.num_kv_heads + x.kvh) * kBlockSize;
+      flag_error(p.errors, PKV_DEVERR_BLOCK_ID);
+      return kv_rows;
+    };
+    auto issue = [&](int t, int row, bool is_v) -> bool {
       const int st = pos % kStages;
       bool good = true;
       if (lane == 0) {
         if (pos >= kStages) good = wait_bar(&sm.empty[st], ((pos / kStages) - 1) & 1, abort);
-        if (good) mbar_arrive_expect_tx(&sm.full[st], kTileBytes);
+        if (good) mbar_arrive_expect_tx(&sm.full[st], mine * (kTileBytes / 8));
       }
       if (!__shfl_sync(kFull, (int)good, 0)) return false;
-      if ((lane >> 3) == (t & 3)) {
+      if ((lane >> 3) == (t & 3) && my_lane) {
         uint8_t* dst = &sm.ring[st][0] + (lane & 7) * (kBlockSize * 128);
         const CUtensorMap* map = is_v ? &tm_v : &tm_k;
         tc::tma_load_2d(dst, map, 0, row, &sm.full[st]);
         tc::tma_load_2d(dst + kHalf, map, 64, row, &sm.full[st]);
       }
       __syncwarp();
-      if (lane == 0) *reinterpret_cast<volatile uint32_t*>(&sm.issued) = pos + 1;
       ++pos;
       return true;
     };
-    while (ok && next_item(p, sm, idx, total, x)) {
-      ck = 0;
-      r_prev = kv_rows;
-      r_cur = rows_for(0);
-      r_next = rows_for(1);
+    // V rows of the partial last block, rows past the context as zeros, into
+    // the tail buffer with the ring's swizzle (0 * NaN would poison the MMA)
+    auto load_tail = [&]() -> bool {
       bool good = true;
-      if (lane == 0) {
+      if (lane == 0 && ntail >= 1) good = wait_bar(&sm.tail_free, (ntail - 1) & 1, abort);
+      if (!__shfl_sync(kFull, (int)good, 0)) return false;
+      const int bi = (x.ctx - 1) / kBlockSize;
+      const int blk = __ldg(p.block_tables + (size_t)x.seq * p.max_blocks_per_seq + bi);
+      const bool bok = blk >= 0 && blk < p.num_blocks;
+      const uint8_t* src =
+          p.v_cache + ((size_t)(bok ? blk : 0) * p.num_kv_heads + x.kvh) * kBlockSize * (kD * 2);
+      const int rows = x.ctx - bi * kBlockSize;
+#pragma unroll
+      for (int i = 0; i < kTailBytes / 16 / 32; ++i) {
+        const int c = lane + 32 * i;
+        const int r = c >> 4, ch = c & 15;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (bok && r < rows) v = __ldg(reinterpret_cast<const uint4*>(src + r * (kD * 2)) + ch);
+        *reinterpret_cast<uint4*>(&sm.tail[0] + (ch >> 3) * (kTailBytes / 2) + r * 128 +
+                                  (((ch & 7) ^ (r & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.tail_full);
+      ++ntail;
+      return true;
+    };
+    while (ok && next_item(p, sm, idx, total, x)) {
+      bool good = true;
+      if (pw == 0 && lane == 0) {
         if (nitem >= 1) good = wait_bar(&sm.q_empty, (nitem - 1) & 1, abort);
         if (good) {
-          mbar_arrive_expect_tx(&sm.q_full, kTileBytes);
-          const int tok = x.q0 + x.t0;
-          tc::tma_load_3d(&sm.q[0], &tm_q, 0, x.kvh * g, tok, &sm.q_full);
-          tc::tma_load_3d(&sm.q[kHalf], &tm_q, 64, x.kvh * g, tok, &sm.q_full);
+          const bool hb = x.nt[1] > 0;
+          mbar_arrive_expect_tx(&sm.q_full, (hb ? 2 : 1) * kTileBytes);
+          for (int qt = 0; qt < (hb ? 2 : 1); ++qt) {
+            const int tok = x.q0 + x.t0[qt];
+            tc::tma_load_3d(&sm.q[qt][0], &tm_q, 0, x.kvh * g, tok, &sm.q_full);
+            tc::tma_load_3d(&sm.q[qt][kHalf], &tm_q, 64, x.kvh * g, tok, &sm.q_full);
+          }
         }
       }
       ok = __shfl_sync(kFull, (int)good, 0) != 0;
-      // ring order = MMA order: K0, then (K_t, V_{t-1}) ..., then V_last
-      if (ok) ok = issue(0, false);
-      for (int t = 1; ok && t < x.nkt; ++t) {
-        ok = issue(t, false);
-        if (ok) ok = issue(t - 1, true);
+      int raw_next = x.nk > 4 ? fetch(1) : kBeyond;
+      int row = to_row(fetch(0));
+      for (int t = 0; ok && t < x.nk; ++t) {
+        if (t > 0 && (t & 3) == 0) {  // next 32 blocks
+          row = to_row(raw_next);
+          raw_next = t + 4 < x.nk ? fetch((t >> 2) + 1) : kBeyond;
+        }
+        ok = issue(t, row, false);
+        if (ok && pw == 0 && t == x.nk - 1 && x.tail_step >= 0) ok = load_tail();
+        if (ok) ok = issue(t, row, true);
       }
-      if (ok) ok = issue(x.nkt - 1, true);
       ++nitem;
     }
     if (!ok && lane == 0) {
@@ -313,67 +376,97 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t y = pos > kStages ? pos - kStages : 0; y < pos; ++y)
         mbar_wait(&sm.full[y % kStages], (y / kStages) & 1, 10000000ull);
     }
-  } else if (warp == 5) {
+  } else if (warp == 8) {
     // ---- MMA issuer --------------------------------------------------------------------
+    // Order per item: S_a(0), S_b(0), then for each key tile t:
+    //   P_a(t) V_t, S_a(t+1), P_b(t) V_t, S_b(t+1)
+    // so each softmax warpgroup works while the tensor pipe serves the other.
     if (lane == 0) {
       int idx = blockIdx.x;
-      uint32_t pos = 0, J = 0;  // ring position, global S-tile counter
-      int nitem = 0;
+      uint32_t pos = 0;
+      uint32_t np[2] = {0, 0};   // P tiles consumed per query tile
+      uint32_t nit[2] = {0, 0};  // items per query tile
+      int nitem = 0, ntail = 0;
       bool ok = true;
       Item x;
-      const uint32_t qa = smem_u32(&sm.q[0]);
-      auto mma_s = [&](uint32_t j) -> bool {
-        const int st = pos % kStages;
-        if (!wait_bar(&sm.full[st], (pos / kStages) & 1, abort)) return false;
-        tc::fence_after_sync();
+      const uint32_t qaddr[2] = {smem_u32(&sm.q[0][0]), smem_u32(&sm.q[1][0])};
+      const uint32_t taddr = smem_u32(&sm.tail[0]);
+      auto acquire = [&](int& st) -> bool {
+        st = pos % kStages;
+        const bool r = wait_bar(&sm.full[st], (pos / kStages) & 1, abort);
+        ++pos;
+        if (r) tc::fence_after_sync();
+        return r;
+      };
+      auto mma_s = [&](int qt, int st) {
         const uint32_t ka = smem_u32(&sm.ring[st][0]);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          tc::mma_f16(tmem + (j & 1) * 128, tc::smem_desc(qa + off, 16, 1024, tc::kLayoutSw128),
+          tc::mma_f16(tmem + qt * 128, tc::smem_desc(qaddr[qt] + off, 16, 1024, tc::kLayoutSw128),
                       tc::smem_desc(ka + off, 16, 1024, tc::kLayoutSw128), kIdescS, kk > 0);
         }
-        tc::mma_commit(&sm.empty[st]);
-        tc::mma_commit(&sm.s_ready[j & 1]);
-        ++pos;
-        return true;
+        tc::mma_commit(&sm.s_ready[qt]);
       };
-      auto mma_pv = [&](uint32_t j, bool first) -> bool {
-        if (!wait_bar(&sm.p_ready[j & 1], (j >> 1) & 1, abort)) return false;
-        const int st = pos % kStages;
-        if (!wait_bar(&sm.full[st], (pos / kStages) & 1, abort)) return false;
+      auto mma_pv = [&](int qt, int st, int t) -> bool {
+        if (!wait_bar(&sm.p_ready[qt], np[qt] & 1, abort)) return false;
+        ++np[qt];
+        if (t == 0 && nit[qt] >= 1 && !wait_bar(&sm.o_free[qt], (nit[qt] - 1) & 1, abort))
+          return false;  // the previous item's O has been read out
         tc::fence_after_sync();
-        const uint32_t pa = smem_u32(&sm.pmat[j & 1][0]);
         const uint32_t va = smem_u32(&sm.ring[st][0]);
+        const int ts = t == x.nk - 1 ? x.tail_step : -1;
 #pragma unroll
         for (int kk = 0; kk < kTileKeys / 16; ++kk) {
-          const uint64_t a = tc::smem_desc(pa + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024,
-                                           tc::kLayoutSw128);
-          const uint64_t b = tc::smem_desc(va + kk * (kBlockSize * 128), kHalf, 1024,
-                                           tc::kLayoutSw128);
-          tc::mma_f16(tmem + 256, a, b, kIdescO, (!first || kk > 0) ? 1u : 0u);
+          const uint64_t b = kk == ts
+                                 ? tc::smem_desc(taddr, kTailBytes / 2, 1024, tc::kLayoutSw128)
+                                 : tc::smem_desc(va + kk * (kBlockSize * 128), kHalf, 1024,
+                                                 tc::kLayoutSw128);
+          mma_f16_tmem_a(tmem + kColO + qt * 128, tmem + qt * 128 + kk * 8, b, kIdescO,
+                         (t | kk) != 0);
         }
-        tc::mma_commit(&sm.empty[st]);
-        tc::mma_commit(&sm.o_done[j & 1]);
-        ++pos;
+        if (t == x.nkt[qt] - 1) tc::mma_commit(&sm.o_done[qt]);
         return true;
       };
       while (ok && next_item(p, sm, idx, total, x)) {
-        if (!wait_bar(&sm.q_full, nitem & 1, abort)) { ok = false; break; }
-        const uint32_t j0 = J;
-        ok = mma_s(J++);
-        for (int t = 1; ok && t < x.nkt; ++t) {
-          ok = mma_s(J++);
-          if (t == x.nkt - 1 && ok) tc::mma_commit(&sm.q_empty);
-          if (ok && t == 1 && nitem >= 1)
-            ok = wait_bar(&sm.o_free, (nitem - 1) & 1, abort);  // previous O read out
-          if (ok) ok = mma_pv(j0 + t - 1, t == 1);
+        const bool hb = x.nt[1] > 0;
+        int kst = 0, vst = 0;
+        ok = wait_bar(&sm.q_full, nitem & 1, abort);
+        if (ok) tc::fence_after_sync();
+        if (ok) ok = acquire(kst);
+        if (ok) {
+          mma_s(0, kst);
+          if (hb) mma_s(1, kst);
+          tc::mma_commit(&sm.empty[kst]);
+          if (x.nk == 1) tc::mma_commit(&sm.q_empty);
         }
-        if (ok && x.nkt == 1) {
-          tc::mma_commit(&sm.q_empty);
-          if (nitem >= 1) ok = wait_bar(&sm.o_free, (nitem - 1) & 1, abort);
+        for (int t = 0; ok && t < x.nk; ++t) {
+          const bool more = t + 1 < x.nk;
+          ok = acquire(vst);
+          if (ok && t == x.nk - 1 && x.tail_step >= 0) {
+            ok = wait_bar(&sm.tail_full, ntail & 1, abort);
+            if (ok) tc::fence_after_sync();
+          }
+          if (ok && t < x.nkt[0]) ok = mma_pv(0, vst, t);
+          if (ok && more) {
+            ok = acquire(kst);
+            if (ok && t + 1 < x.nkt[0]) mma_s(0, kst);
+          }
+          if (ok && hb) ok = mma_pv(1, vst, t);
+          if (!ok) break;
+          tc::mma_commit(&sm.empty[vst]);
+          if (more) {
+            if (hb) mma_s(1, kst);
+            tc::mma_commit(&sm.empty[kst]);
+            if (t + 1 == x.nk - 1) tc::mma_commit(&sm.q_empty);
+          }
         }
-        if (ok) ok = mma_pv(j0 + x.nkt - 1, x.nkt == 1);
+        if (ok && x.tail_step >= 0) {
+          tc::mma_commit(&sm.tail_free);
+          ++ntail;
+        }
+        ++nit[0];
+        if (hb) ++nit[1];
         ++nitem;
       }
       if (!ok) flag_error(p.errors, PKV_DEVERR_TIMEOUT);
@@ -381,134 +474,120 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&sm.mma_done, 0, 100000000ull);
     }
   } else {
-    // ---- softmax + epilogue (warps 0-3, thread = row = TMEM lane) ----------------------------
-    const int tid = threadIdx.x;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // ---- softmax + epilogue: warpgroup qt = 0 (tile a) or 1 (tile b) --------------------
+    const int qt = warp >> 2;
+    const int tid = threadIdx.x & 127;  // row = TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_col = tmem + lane_off + qt * 128;
+    const uint32_t o_col = tmem + lane_off + kColO + qt * 128;
     const float qs = p.q_scale;
     using OutT = typename QT::T;
+    // Scores are scaled inside the exponent: exp2(s * |q_scale| - m) with m the
+    // scaled running max.  A negative scale is folded in by negating the
+    // scores; a zero scale is taken as 1e-30 (exp2 of s * 1e-30 rounds to 1).
+    const bool neg = qs < 0.0f;
+    const float qa = fmaxf(fabsf(qs), 1e-30f);
     int idx = blockIdx.x;
-    uint32_t J = 0, pos = 0;
+    uint32_t ns = 0, nit = 0;  // S tiles and items of this query tile
     bool ok = true;
     Item x;
     while (ok && next_item(p, sm, idx, total, x)) {
-      const int tok = tid / g;  // token within the tile
-      const bool valid = tid < x.nt * g;
-      const int qpos = x.pos0 + tok;
-      float m_run = -INFINITY, l = 0.0f;
-      const uint32_t item_pos = pos;  // ring position of this item's K0
-      pos += 2 * x.nkt;
-      for (int t = 0; t < x.nkt; ++t, ++J) {
-        ok = all_softmax(wait_bar(&sm.s_ready[J & 1], (J >> 1) & 1, abort));
+      if (x.nt[qt] == 0) continue;  // no tile b in this item
+      const int tok = tid / g;      // token within the tile
+      // rows past the tile's tokens compute on whatever Q holds there; their
+      // output is never stored
+      const bool valid = tid < x.nt[qt] * g;
+      const int qpos = x.pos0[qt] + tok;
+      float m_run = -INFINITY;
+      float l8[8];  // partial row sums (independent chains)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) l8[i] = 0.0f;
+      for (int t = 0; t < x.nkt[qt]; ++t, ++ns) {
+        ok = all_group(wait_bar(&sm.s_ready[qt], ns & 1, abort), qt);
         if (!ok) break;
         tc::fence_after_sync();
         float sv[kTileKeys];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tc::tmem_ld32(tmem + lane_off + (J & 1) * 128 + 32 * c, sv + 32 * c);
+        for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_col + 32 * c, sv + 32 * c);
         tc::tmem_wait_ld();
         const int kbase = t * kTileKeys;
-        float mt = -INFINITY;
+        if (neg) {
 #pragma unroll
-        for (int c = 0; c < kTileKeys; ++c) {
-          const bool vis = valid && kbase + c <= qpos;
-          sv[c] = vis ? sv[c] * qs : -INFINITY;
-          mt = fmaxf(mt, sv[c]);
+          for (int c = 0; c < kTileKeys; ++c) sv[c] = -sv[c];
         }
-        // move the running max (and rescale O) only on a large increase
-        const bool need = valid && (mt > m_run + kRescaleAt);
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+        if (kbase + kTileKeys - 1 > x.pos0[qt]) {
+          // the causal boundary crosses this tile: hidden keys become -inf
+#pragma unroll
+          for (int c = 0; c < kTileKeys; ++c) {
+            sv[c] = kbase + c <= qpos ? sv[c] : -INFINITY;
+            mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kTileKeys; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
+        }
+        const float mt =
+            fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * qa;
+        // move the running max (and rescale O) only on a large increase; O is
+        // complete up to tile t-1 (S of tile t was issued after its product)
+        const bool need = mt > m_run + kRescaleAt;
         float alpha = 1.0f;
         if (need) {
           alpha = (t == 0) ? 0.0f : fast_exp2(m_run - mt);
           m_run = mt;
-          l *= alpha;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) l8[i] *= alpha;
         }
+        // P over the first 64 columns of S: keys 2c and 2c+1 in column c
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          float pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int k0 = h * 32 + 2 * c;
+            const float e0 = fast_exp2(fmaf(sv[k0], qa, -m_run));
+            const float e1 = fast_exp2(fmaf(sv[k0 + 1], qa, -m_run));
+            l8[(2 * c) & 7] += e0;
+            l8[(2 * c + 1) & 7] += e1;
+            pk[c] = __uint_as_float(pack2<QT>(e0, e1));
+          }
+          tc::tmem_st16(s_col + 16 * h, pk);
+        }
+        // the product of tile t adds onto O: rescale it first when a row's max moved
         if (t > 0 && __any_sync(kFull, need)) {
-          // O must be complete up to tile t-1 before it is rescaled in place
-          bool w = wait_bar(&sm.o_done[(J - 1) & 1], ((J - 1) >> 1) & 1, abort);
-          if (!__all_sync(kFull, w)) { ok = false; }
-          if (ok) {
-            tc::fence_after_sync();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float ov[32];
+            tc::tmem_ld32(o_col + 32 * c, ov);
+            tc::tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              float ov[32];
-              tc::tmem_ld32(tmem + lane_off + 256 + 32 * c, ov);
-              tc::tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-              tc::tmem_st32(tmem + lane_off + 256 + 32 * c, ov);
-            }
-            tc::tmem_wait_st();
+            for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+            tc::tmem_st32(o_col + 32 * c, ov);
           }
         }
-        ok = all_softmax(ok);
-        if (!ok) break;
-        // P buffer J&1 was last read by the product of tile J-2
-        if (J >= 2) {
-          ok = all_softmax(wait_bar(&sm.o_done[J & 1], ((J - 2) >> 1) & 1, abort));
-          if (!ok) break;
-        }
-        uint8_t* prow = &sm.pmat[J & 1][0] + tid * 128;
-        const int sw = tid & 7;
-#pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {  // 16-byte chunks of 8 keys
-          float e[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float v = sv[ch * 8 + i];
-            e[i] = valid ? fast_exp2(v - m_run) : 0.0f;
-            l += e[i];
-          }
-          uint4 w;
-          w.x = pack2<QT>(e[0], e[1]);
-          w.y = pack2<QT>(e[2], e[3]);
-          w.z = pack2<QT>(e[4], e[5]);
-          w.w = pack2<QT>(e[6], e[7]);
-          const int half = ch >> 3, c16 = (ch & 7) ^ sw;
-          *reinterpret_cast<uint4*>(prow + half * kHalf + c16 * 16) = w;
-        }
-        // V rows past the context in the last block are garbage (0 * NaN = NaN
-        // inside the MMA): zero them once that tile has landed
-        const int last = x.ctx - 1;
-        const int tail = x.ctx & (kBlockSize - 1);
-        if (t == x.nkt - 1 && tail && last >= kbase && last < kbase + kTileKeys) {
-          const uint32_t vpos = item_pos + 2 * x.nkt - 1;
-          bool w = true;
-          const uint64_t t0 = globaltimer_ns();
-          while (*reinterpret_cast<volatile uint32_t*>(&sm.issued) <= vpos) {
-            if (*abort || globaltimer_ns() - t0 > 2000000000ull) {
-              *abort = 1;
-              w = false;
-              break;
-            }
-          }
-          if (w) w = wait_bar(&sm.full[vpos % kStages], (vpos / kStages) & 1, abort);
-          ok = all_softmax(w);
-          if (!ok) break;
-          const int jb = (last - kbase) / kBlockSize;
-          const int rows = kBlockSize - tail;
-          uint8_t* vb = &sm.ring[vpos % kStages][0] + (jb * kBlockSize + tail) * 128;
-          for (int i = tid; i < rows * 2 * 8; i += 128) {
-            const int half = i / (rows * 8), r = (i / 8) % rows, c = i % 8;
-            reinterpret_cast<uint4*>(vb + half * kHalf + r * 128)[c] = make_uint4(0, 0, 0, 0);
-          }
-        }
-        fence_proxy_async_smem();
+        tc::tmem_wait_st();
         tc::fence_before_sync();
-        tc::named_sync(1, 128);
-        if (tid == 0) mbar_arrive(&sm.p_ready[J & 1]);
+        tc::named_sync(1 + qt, 128);
+        if (tid == 0) mbar_arrive(&sm.p_ready[qt]);
       }
       if (!ok) break;
       // ---- epilogue: O / l --------------------------------------------------------------
-      const uint32_t jl = J - 1;
-      ok = all_softmax(wait_bar(&sm.o_done[jl & 1], (jl >> 1) & 1, abort));
+      ok = all_group(wait_bar(&sm.o_done[qt], nit & 1, abort), qt);
       if (!ok) break;
       tc::fence_after_sync();
+      const float l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
       const float inv = valid ? 1.0f / l : 0.0f;
       OutT* orow = static_cast<OutT*>(p.out) +
-                   ((size_t)(x.q0 + x.t0 + tok) * p.num_heads + (size_t)x.kvh * g + tid % g) * kD;
-#pragma unroll
+                   ((size_t)(x.q0 + x.t0[qt] + tok) * p.num_heads + (size_t)x.kvh * g + tid % g) *
+                       kD;
+#pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float ov[32];
-        tc::tmem_ld32(tmem + lane_off + 256 + 32 * c, ov);
+        tc::tmem_ld32(o_col + 32 * c, ov);
         tc::tmem_wait_ld();
         if (valid) {
 #pragma unroll
@@ -523,15 +602,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc::fence_before_sync();
-      tc::named_sync(1, 128);
-      if (tid == 0) mbar_arrive(&sm.o_free);
+      tc::named_sync(1 + qt, 128);
+      if (tid == 0) mbar_arrive(&sm.o_free[qt]);
+      ++nit;
     }
     if (!ok && tid == 0) flag_error(p.errors, PKV_DEVERR_TIMEOUT);
   }
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 8) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
@@ -550,7 +630,7 @@ int launch_typed(const AttnParams& p, int total_q, cudaStream_t stream) {
   const size_t smem = sizeof(Smem) + 1024;
   static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory budget of one CTA");
   static_assert(offsetof(Smem, ring) % 1024 == 0 && offsetof(Smem, q) % 1024 == 0 &&
-                    offsetof(Smem, pmat) % 1024 == 0,
+                    offsetof(Smem, tail) % 1024 == 0,
                 "swizzled buffers must start on 1024-byte boundaries");
   auto kern = prefill_tc_kernel<QT>;
   static bool configured = false;
@@ -560,9 +640,10 @@ int launch_typed(const AttnParams& p, int total_q, cudaStream_t stream) {
       return PKV_ERR_CUDA;
     configured = true;
   }
-  // an upper bound of the items: every sequence's tiles, times the KV heads
-  const long long rows = (long long)total_q * p.group + (long long)p.num_seqs * (kRowsM - 1);
-  const long long items = rows / kRowsM * p.num_kv_heads;
+  // an upper bound of the items: every sequence's tile pairs, times the KV heads
+  const long long tiles = ((long long)total_q * p.group + (long long)p.num_seqs * (kRowsM - 1)) /
+                          kRowsM;
+  const long long items = (tiles + p.num_seqs) / 2 * p.num_kv_heads;
   int grid = sm_count();
   if (items < grid) grid = (int)(items > 0 ? items : 1);
   kern<<<grid, kThreads, smem, stream>>>(p, tk, tv, tq, (int)kv_rows);
