@@ -398,13 +398,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (r) tc::fence_after_sync();
         return r;
       };
+      // Operand descriptors are built once; a step moves the start address
+      // field (bytes / 16 in the low bits, no carry below 256 KB).
+      const uint64_t dq[2] = {tc::smem_desc(qaddr[0], 16, 1024, tc::kLayoutSw128),
+                              tc::smem_desc(qaddr[1], 16, 1024, tc::kLayoutSw128)};
+      const uint64_t dk0 = tc::smem_desc(smem_u32(&sm.ring[0][0]), 16, 1024, tc::kLayoutSw128);
+      const uint64_t dv0 =
+          tc::smem_desc(smem_u32(&sm.ring[0][0]), kHalf, 1024, tc::kLayoutSw128);
+      const uint64_t dtail = tc::smem_desc(taddr, kTailBytes / 2, 1024, tc::kLayoutSw128);
       auto mma_s = [&](int qt, int st) {
-        const uint32_t ka = smem_u32(&sm.ring[st][0]);
+        const uint64_t dk = dk0 + (uint64_t)(st * (kTileBytes >> 4));
+        const uint64_t dqa = dq[qt];
+        const uint32_t d = tmem + qt * 128;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          tc::mma_f16(tmem + qt * 128, tc::smem_desc(qaddr[qt] + off, 16, 1024, tc::kLayoutSw128),
-                      tc::smem_desc(ka + off, 16, 1024, tc::kLayoutSw128), kIdescS, kk > 0);
+          const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+          tc::mma_f16(d, dqa + off, dk + off, kIdescS, kk > 0);
         }
         tc::mma_commit(&sm.s_ready[qt]);
       };
@@ -414,16 +423,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t == 0 && nit[qt] >= 1 && !wait_bar(&sm.o_free[qt], (nit[qt] - 1) & 1, abort))
           return false;  // the previous item's O has been read out
         tc::fence_after_sync();
-        const uint32_t va = smem_u32(&sm.ring[st][0]);
+        const uint64_t dv = dv0 + (uint64_t)(st * (kTileBytes >> 4));
         const int ts = t == x.nk - 1 ? x.tail_step : -1;
+        const uint32_t d = tmem + kColO + qt * 128, a = tmem + qt * 128;
 #pragma unroll
         for (int kk = 0; kk < kTileKeys / 16; ++kk) {
-          const uint64_t b = kk == ts
-                                 ? tc::smem_desc(taddr, kTailBytes / 2, 1024, tc::kLayoutSw128)
-                                 : tc::smem_desc(va + kk * (kBlockSize * 128), kHalf, 1024,
-                                                 tc::kLayoutSw128);
-          mma_f16_tmem_a(tmem + kColO + qt * 128, tmem + qt * 128 + kk * 8, b, kIdescO,
-                         (t | kk) != 0);
+          const uint64_t b = kk == ts ? dtail : dv + (uint64_t)((kk * (kBlockSize * 128)) >> 4);
+          mma_f16_tmem_a(d, a + kk * 8, b, kIdescO, (t | kk) != 0);
         }
         if (t == x.nkt[qt] - 1) tc::mma_commit(&sm.o_done[qt]);
         return true;
