@@ -19,11 +19,15 @@
 //
 // Warp roles: 0-3 softmax + epilogue (thread = TMEM lane); 4 K producer (and
 // the query on 16-bit caches); 5 TMEM owner + MMA issuer; 6 V producer; then
-// 7 the tail loader (16-bit caches) or 7-10 the query converters and tail
-// loader (E4M3 caches).  K and V tiles stream through separate shared-memory
-// rings, so K tiles of later items keep arriving (and their scores keep being
-// computed) while V tiles of the current item wait for its softmax.  TMEM
-// holds two items.
+// on 16-bit caches 7 the tail loader (and 8-9 second K and V producers with
+// at most 8 heads per group), on E4M3 caches 7-10 the query converters and
+// tail loader.  One warp issuing 16-row boxes moves about 31 GB/s per SM, two
+// per ring more, so the 16-bit rings' boxes are spread over two warps where
+// registers allow (the E4M3 kernel is bound by its softmax warps, and second
+// producers bought it nothing).  K and V tiles stream through separate
+// shared-memory rings, so K tiles of later items keep arriving (and their
+// scores keep being computed) while V tiles of the current item wait for its
+// softmax.  TMEM holds two items.
 //
 // 16-bit tiles are [2 halves][128 rows][64 dims] with the 128-byte swizzle,
 // filled by two 16-row TMA boxes per block; the same layout serves K as a
@@ -55,7 +59,10 @@
 namespace pkv {
 namespace {
 
-constexpr int tc_threads(bool fp8) { return fp8 ? 352 : 256; }
+// producer warps per ring, and threads: the 16-bit, 16-head variant needs
+// more registers than 320 threads leave
+constexpr int tc_prod(bool g16, bool fp8) { return (fp8 || g16) ? 1 : 2; }
+constexpr int tc_threads(bool g16, bool fp8) { return fp8 ? 352 : (g16 ? 256 : 320); }
 constexpr int kTileKeys = 128;
 constexpr int kPart = 512;
 constexpr int kTilesPerPart = kPart / kTileKeys;
@@ -191,14 +198,18 @@ __device__ __forceinline__ bool all_of_group(bool ok) {
 __device__ __forceinline__ bool all_softmax(bool ok) { return all_of_group<1>(ok); }
 
 template <class QT, bool G16, bool FP8>
-__global__ void __launch_bounds__(tc_threads(FP8), 1)
+__global__ void __launch_bounds__(tc_threads(G16, FP8), 1)
     paged_decode_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
                            const __grid_constant__ CUtensorMap tm_q, int kv_rows) {
   extern __shared__ uint8_t smem_raw[];
   using L = Layout<G16, FP8>;
   constexpr int KS = L::kKStages, VS = L::kVStages;
-  constexpr int kThreads = tc_threads(FP8);
+  constexpr int kThreads = tc_threads(G16, FP8);
+  constexpr int kProd = tc_prod(G16, FP8);
+  // second producers of the K and V rings
+  constexpr int kWarpK1 = kProd == 2 ? 8 : -1;
+  constexpr int kWarpV1 = kProd == 2 ? 9 : -1;
   Smem<G16, FP8>& sm = *reinterpret_cast<Smem<G16, FP8>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -211,11 +222,11 @@ __global__ void __launch_bounds__(tc_threads(FP8), 1)
   // ---- set-up -------------------------------------------------------------------------
   if (threadIdx.x == 0) {
     for (int s = 0; s < KS; ++s) {
-      mbar_init(&sm.kfull[s], 1);
+      mbar_init(&sm.kfull[s], kProd);
       mbar_init(&sm.kempty[s], 1);
     }
     for (int s = 0; s < VS; ++s) {
-      mbar_init(&sm.vfull[s], 1);
+      mbar_init(&sm.vfull[s], kProd);
       mbar_init(&sm.vempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -285,7 +296,7 @@ __global__ void __launch_bounds__(tc_threads(FP8), 1)
     }
     if (tid == kThreads - 1) sm.seq_pack[S] = (base + incl) << kLenBits;
   }
-  // padded rows of P stay zero for the whole kernel
+  // P starts as zeros (every row a tile multiplies is rewritten per item)
   for (int i = threadIdx.x; i < 2 * L::kPBytes / 16; i += kThreads)
     reinterpret_cast<uint4*>(&sm.pmat[0][0])[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
@@ -296,10 +307,13 @@ __global__ void __launch_bounds__(tc_threads(FP8), 1)
   volatile int* abort = &sm.abort;
   const int total = (sm.seq_pack[p.num_rows] >> kLenBits) * p.num_kv_heads;
 
-  if (warp == 4 || warp == 6) {
-    // ---- TMA producers: warp 4 K (and the 16-bit query), warp 6 V -----------------------
-    // Lane j owns block j of an item's 32-block partition.
-    const bool is_v = warp == 6;
+  if (warp == 4 || warp == 6 || warp == kWarpK1 || warp == kWarpV1) {
+    // ---- TMA producers: K (warp 4, and the 16-bit query) and V (warp 6) --------------------
+    // Lane j reads the table entry of block j of an item's 32-block partition;
+    // producer pi of a ring issues the boxes of blocks j with j % kProd == pi.
+    const bool is_v = warp == 6 || warp == kWarpV1;
+    const int pi = (warp == 4 || warp == 6) ? 0 : 1;
+    const bool my_block = (lane & 7) % kProd == pi;
     const CUtensorMap* map = is_v ? &tm_v : &tm_k;
     uint64_t* full = is_v ? sm.vfull : sm.kfull;
     uint64_t* empty = is_v ? sm.vempty : sm.kempty;
@@ -319,7 +333,7 @@ __global__ void __launch_bounds__(tc_threads(FP8), 1)
                               x.part * (kPart / kBlockSize) + lane);
         if (blk >= 0 && blk < p.num_blocks)
           row = (blk * p.num_kv_heads + x.kvh) * kBlockSize;
-        else if (!is_v)
+        else if (!is_v && pi == 0)
           flag_error(p.errors, PKV_DEVERR_BLOCK_ID);
       }
       return row;
@@ -345,10 +359,10 @@ __global__ void __launch_bounds__(tc_threads(FP8), 1)
         bool good = true;
         if (lane == 0) {
           if (pos >= nst) good = wait_bar(&empty[st], ((pos / nst) - 1) & 1, abort);
-          if (good) mbar_arrive_expect_tx(&full[st], L::kTileBytes);
+          if (good) mbar_arrive_expect_tx(&full[st], L::kTileBytes / kProd);
         }
         if (!__shfl_sync(kFull, (int)good, 0)) return false;
-        if ((lane >> 3) == t) {
+        if ((lane >> 3) == t && my_block) {
           uint8_t* dst = ring + (size_t)st * L::kTileBytes + (lane & 7) * (kBlockSize * 128);
           tc::tma_load_2d(dst, map, 0, row, &full[st]);
           if (!FP8) tc::tma_load_2d(dst + kHalfBytes, map, 64, row, &full[st]);
@@ -364,7 +378,7 @@ __global__ void __launch_bounds__(tc_threads(FP8), 1)
       // block rows are read one item ahead of their first use
       const bool has_n = next_item(p, sm, idx, total, nxt);
       const int row_nxt = has_n ? block_row(nxt) : kv_rows;
-      if (!is_v) ok = load_q(cur, it);
+      if (!is_v && pi == 0) ok = load_q(cur, it);
       if (ok) ok = load_tiles(cur, row_cur);
       cur = nxt;
       row_cur = row_nxt;
@@ -488,7 +502,7 @@ __global__ void __launch_bounds__(tc_threads(FP8), 1)
       tc::mma_commit(&sm.mma_done);
       mbar_wait(&sm.mma_done, 0, 100000000ull);
     }
-  } else if (warp >= 7) {
+  } else if (warp == 7 || (FP8 && warp > 7)) {
     // ---- tail loader (16-bit: warp 7) / query converters + tail loader (E4M3: 7-10) -----
     constexpr int kGroup = FP8 ? 128 : 32;
     const int gtid = threadIdx.x - 224;
@@ -744,7 +758,11 @@ __global__ void __launch_bounds__(tc_threads(FP8), 1)
             for (int h = 0; h < 8; ++h) s[t][h] += s[t][h + 8];
         }
       }
-      // running max per head over this thread's keys, then over the CTA
+      // Running max per head over this thread's keys, then over the CTA.  All
+      // kRows heads are reduced and written to P: heads past the group hold
+      // finite scores (the next group's queries, or zeros past the tensor) and
+      // are never stored, and loops without per-head branches let the
+      // independent shuffle chains of the heads interleave.
       float mx[16];
 #pragma unroll
       for (int h = 0; h < L::kRows; ++h) mx[h] = -INFINITY;
@@ -758,21 +776,20 @@ __global__ void __launch_bounds__(tc_threads(FP8), 1)
         }
       }
 #pragma unroll
-      for (int h = 0; h < L::kRows; ++h) {
-        if (h < p.group) {
+      for (int o = 16; o; o >>= 1)
 #pragma unroll
-          for (int o = 16; o; o >>= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], o));
-          if (lane == 0) sm.red_max[warp][h] = mx[h];
-        }
+        for (int h = 0; h < L::kRows; ++h) mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], o));
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < L::kRows; ++h) sm.red_max[warp][h] = mx[h];
       }
       tc::named_sync(1, 128);
       float sum[16];
 #pragma unroll
       for (int h = 0; h < L::kRows; ++h) {
         sum[h] = 0.0f;
-        if (h < p.group)
-          mx[h] = fmaxf(fmaxf(sm.red_max[0][h], sm.red_max[1][h]),
-                        fmaxf(sm.red_max[2][h], sm.red_max[3][h]));
+        mx[h] = fmaxf(fmaxf(sm.red_max[0][h], sm.red_max[1][h]),
+                      fmaxf(sm.red_max[2][h], sm.red_max[3][h]));
       }
       // P[h][key] in the K-major core-matrix layout (8 keys per 16-byte row of a
       // 16-bit core matrix, 16 keys for E4M3), and its row sums
@@ -783,45 +800,41 @@ __global__ void __launch_bounds__(tc_threads(FP8), 1)
           const int key = t * kTileKeys + tid;
 #pragma unroll
           for (int h = 0; h < L::kRows; h += 2) {
-            if (h < p.group) {
-              const float e0 = fast_exp2(s[t][h] - mx[h]);
-              const float e1 = h + 1 < p.group ? fast_exp2(s[t][h + 1] - mx[h + 1]) : 0.0f;
-              sum[h] += e0;
-              sum[h + 1] += e1;
-              if constexpr (FP8) {
-                // E4M3 with a 2^8 scale (weights are <= 1)
-                const __nv_fp8x2_storage_t q2 =
-                    __nv_cvt_float2_to_fp8x2(make_float2(e0 * 256.0f, e1 * 256.0f),
-                                             __NV_SATFINITE, __NV_E4M3);
-                uint8_t* c8 =
-                    pm + (key >> 4) * 128 + (h >> 3) * L::kPSbo + (h & 7) * 16 + (key & 15);
-                c8[0] = (uint8_t)(q2 & 0xffu);
-                if (h + 1 < p.group) c8[16] = (uint8_t)(q2 >> 8);
+            const float e0 = fast_exp2(s[t][h] - mx[h]);
+            const float e1 = fast_exp2(s[t][h + 1] - mx[h + 1]);
+            sum[h] += e0;
+            sum[h + 1] += e1;
+            if constexpr (FP8) {
+              // E4M3 with a 2^8 scale (weights are <= 1)
+              const __nv_fp8x2_storage_t q2 = __nv_cvt_float2_to_fp8x2(
+                  make_float2(e0 * 256.0f, e1 * 256.0f), __NV_SATFINITE, __NV_E4M3);
+              uint8_t* c8 = pm + (key >> 4) * 128 + (h >> 3) * L::kPSbo + (h & 7) * 16 + (key & 15);
+              c8[0] = (uint8_t)(q2 & 0xffu);
+              c8[16] = (uint8_t)(q2 >> 8);
+            } else {
+              uint32_t pr;
+              if constexpr (std::is_same<QT, BF16>::value) {
+                __nv_bfloat162 v2 = __floats2bfloat162_rn(e0, e1);
+                pr = *reinterpret_cast<uint32_t*>(&v2);
               } else {
-                uint32_t pr;
-                if constexpr (std::is_same<QT, BF16>::value) {
-                  __nv_bfloat162 v2 = __floats2bfloat162_rn(e0, e1);
-                  pr = *reinterpret_cast<uint32_t*>(&v2);
-                } else {
-                  __half2 v2 = __floats2half2_rn(e0, e1);
-                  pr = *reinterpret_cast<uint32_t*>(&v2);
-                }
-                uint8_t* c0 = pm + (key >> 3) * 128 + (key & 7) * 2 + (h >> 3) * kPGroupStride +
-                              (h & 7) * 16;
-                *reinterpret_cast<uint16_t*>(c0) = (uint16_t)(pr & 0xffffu);
-                if (h + 1 < p.group) *reinterpret_cast<uint16_t*>(c0 + 16) = (uint16_t)(pr >> 16);
+                __half2 v2 = __floats2half2_rn(e0, e1);
+                pr = *reinterpret_cast<uint32_t*>(&v2);
               }
+              uint8_t* c0 = pm + (key >> 3) * 128 + (key & 7) * 2 + (h >> 3) * kPGroupStride +
+                            (h & 7) * 16;
+              *reinterpret_cast<uint16_t*>(c0) = (uint16_t)(pr & 0xffffu);
+              *reinterpret_cast<uint16_t*>(c0 + 16) = (uint16_t)(pr >> 16);
             }
           }
         }
       }
 #pragma unroll
-      for (int h = 0; h < L::kRows; ++h) {
-        if (h < p.group) {
+      for (int o = 16; o; o >>= 1)
 #pragma unroll
-          for (int o = 16; o; o >>= 1) sum[h] += __shfl_xor_sync(kFull, sum[h], o);
-          if (lane == 0) sm.red_sum[warp][h] = sum[h];
-        }
+        for (int h = 0; h < L::kRows; ++h) sum[h] += __shfl_xor_sync(kFull, sum[h], o);
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < L::kRows; ++h) sm.red_sum[warp][h] = sum[h];
       }
       fence_proxy_async_smem();
       tc::fence_before_sync();
@@ -910,7 +923,7 @@ int launch_tc_typed(const AttnParams& p, cudaStream_t stream) {
     int grid = sm_count();
     if (items < grid) grid = (int)items;
     if (grid < 1) grid = 1;
-    kern<<<grid, tc_threads(FP8), smem, stream>>>(c, tk, tv, tq, (int)kv_rows);
+    kern<<<grid, tc_threads(G16, FP8), smem, stream>>>(c, tk, tv, tq, (int)kv_rows);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   }
   return PKV_OK;
