@@ -211,6 +211,53 @@ int pkv_paged_attention_prefill_chunk(void* out, const void* q, const void* k_ca
                                       uint32_t* device_errors, void* stream);
 
 /*
+ * Bytes of device workspace pkv_paged_attention_decode_cascade needs.
+ */
+size_t pkv_cascade_workspace_size(int num_seqs, int num_heads, int head_dim,
+                                  int max_context_len, int max_prefix_len);
+
+/*
+ * Cascade (shared-prefix) decode: the same result as pkv_paged_attention_decode,
+ * for a batch in which groups of sequences share a prompt's blocks by
+ * reference (parallel samples of one prompt).  Each shared block is read once
+ * per group instead of once per sequence: every member's query attends the
+ * shared prefix in one pass, each sequence attends its own keys in a second,
+ * and the partial results are combined by a log-sum-exp merge.
+ * Sources: openeuler.csdn.net PagedAttention notes, "vLLM - PagedAttention",
+ * "机制 2：写时复制（Copy-on-Write）" (parallel samples of one prompt share its
+ * physical blocks with a reference count, private blocks only from the
+ * diverging point); devpress.csdn.net vLLM overview, "9、FlashAttention (4)"
+ * (partial results over disjoint key sets combined by running max and sum of
+ * exponentials).
+ *
+ *   group_start  [num_groups + 1] int32: group g is the sequences
+ *         group_start[g] .. group_start[g+1]-1 (consecutive; [0] = 0,
+ *         [num_groups] = num_seqs, non-decreasing).
+ *   prefix_lens  [num_seqs] int32: the shared prefix of each sequence, in
+ *         tokens: a multiple of 16, at most its context, equal for the
+ *         members of a group, whose block tables agree on those blocks (the
+ *         prefix is read through the group's first member).  0 = nothing
+ *         shared.  A length that is not whole blocks or exceeds the context is
+ *         cut back and flagged PKV_DEVERR_CONTEXT.
+ *   max_prefix_len  an upper bound of prefix_lens (sizes the workspace).
+ *   workspace  at least pkv_cascade_workspace_size(...) bytes, 256-byte
+ *         aligned; never NULL for num_seqs > 0.
+ *   Supported: 16-bit caches (kv_dtype == q_dtype), head_dim 128, 2..16 query
+ *   heads per KV head dividing 128, at most 1024 groups; otherwise
+ *   PKV_ERR_UNSUPPORTED.  Other arguments as for pkv_paged_attention_decode.
+ */
+int pkv_paged_attention_decode_cascade(void* out, const void* q, const void* k_cache,
+                                       const void* v_cache, const int32_t* block_tables,
+                                       const int32_t* context_lens, const int32_t* group_start,
+                                       const int32_t* prefix_lens, int num_seqs, int num_groups,
+                                       int num_heads, int num_kv_heads, int head_dim,
+                                       int block_size, int max_blocks_per_seq, int num_blocks,
+                                       int max_context_len, int max_prefix_len, float scale,
+                                       pkv_dtype q_dtype, pkv_dtype kv_dtype, float k_scale,
+                                       float v_scale, void* workspace, size_t workspace_bytes,
+                                       uint32_t* device_errors, void* stream);
+
+/*
  * Synchronises `stream`, reads the device error word, clears it, and returns
  * PKV_OK, PKV_ERR_TIMEOUT (a wait gave up) or PKV_ERR_DEVICE (any other bit);
  * PKV_ERR_CUDA if the stream reports an error.  *bits_out (may be NULL)

@@ -82,6 +82,11 @@ def load():
             lib.pkv_paged_attention_decode_noalloc.restype = _I
             lib.pkv_paged_attention_decode_noalloc.argtypes = (
                 [_P] * 6 + [_I] * 8 + [_F, _I, _I, _F, _F, _I, _P, _P])
+            lib.pkv_cascade_workspace_size.restype = _SZ
+            lib.pkv_cascade_workspace_size.argtypes = [_I] * 5
+            lib.pkv_paged_attention_decode_cascade.restype = _I
+            lib.pkv_paged_attention_decode_cascade.argtypes = (
+                [_P] * 8 + [_I] * 10 + [_F, _I, _I, _F, _F, _P, _SZ, _P, _P])
             lib.pkv_check_errors.restype = _I
             lib.pkv_check_errors.argtypes = [_P, _P, _P]
             _lib = lib
@@ -189,6 +194,39 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
         _dtype_code(k_cache), k_scale, v_scale, partition_size, _ptr(ws), wsb,
         _ptr(device_errors), _stream(stream))
     _check("pkv_paged_attention_decode", rc)
+    return out
+
+
+def cascade_workspace_size(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,
+                           max_prefix_len: int) -> int:
+    return load().pkv_cascade_workspace_size(num_seqs, num_heads, head_dim, max_context_len,
+                                             max_prefix_len)
+
+
+def paged_attention_decode_cascade(out, q, k_cache, v_cache, block_tables, context_lens,
+                                   group_start, prefix_lens, scale: float,
+                                   max_context_len: int | None = None,
+                                   max_prefix_len: int | None = None, workspace=None,
+                                   device_errors=None, stream=None):
+    """Decode attention of q ([S, H, D]) over the paged caches into out, reading
+    each group's shared prefix once (see pkv_paged_attention_decode_cascade in
+    include/pagedkv.h).  group_start: [G + 1] int32; prefix_lens: [S] int32."""
+    _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, group_start, prefix_lens,
+               device_errors)
+    S, H, D = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if S else 0
+    if max_prefix_len is None:
+        max_prefix_len = int(prefix_lens.max().item()) if S else 0
+    need = cascade_workspace_size(S, H, D, max_context_len, max_prefix_len)
+    ws, wsb = _workspace(need, workspace, q.device)
+    rc = load().pkv_paged_attention_decode_cascade(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        _ptr(group_start), _ptr(prefix_lens), S, group_start.numel() - 1, H, hkv, D, bs,
+        block_tables.shape[1], nb, max_context_len, max_prefix_len, scale, _dtype_code(q),
+        _dtype_code(k_cache), 1.0, 1.0, _ptr(ws), wsb, _ptr(device_errors), _stream(stream))
+    _check("pkv_paged_attention_decode_cascade", rc)
     return out
 
 

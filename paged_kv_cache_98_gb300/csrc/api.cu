@@ -10,6 +10,7 @@
 namespace {
 
 constexpr int kDefaultPartition = 512;
+constexpr int kCascadeChunk = 2048;  // keys per partial of the shared-prefix pass
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -256,6 +257,96 @@ int pkv_paged_attention_prefill_chunk(void* out, const void* q, const void* k_ca
   const size_t need = split_workspace((size_t)total_q, num_heads, head_dim, p.max_parts);
   return run_attention(p, q_dtype, kv_dtype, head_dim, scale, k_scale, v_scale, workspace, need,
                        workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t pkv_cascade_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                                  int max_prefix_len) {
+  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||
+      max_prefix_len < 0)
+    return 0;
+  // the shared prefix's chunks, then the sequence's own partitions; the
+  // partials always go through the workspace
+  const int slots = 2 * ((max_prefix_len + kCascadeChunk - 1) / kCascadeChunk) +
+                    parts_for(max_context_len, kDefaultPartition);
+  const size_t heads = (size_t)num_seqs * num_heads * slots;
+  return round_up(heads * sizeof(float), 256) + round_up(heads * head_dim * sizeof(float), 256);
+}
+
+int pkv_paged_attention_decode_cascade(void* out, const void* q, const void* k_cache,
+                                       const void* v_cache, const int32_t* block_tables,
+                                       const int32_t* context_lens, const int32_t* group_start,
+                                       const int32_t* prefix_lens, int num_seqs, int num_groups,
+                                       int num_heads, int num_kv_heads, int head_dim,
+                                       int block_size, int max_blocks_per_seq, int num_blocks,
+                                       int max_context_len, int max_prefix_len, float scale,
+                                       pkv_dtype q_dtype, pkv_dtype kv_dtype, float k_scale,
+                                       float v_scale, void* workspace, size_t workspace_bytes,
+                                       uint32_t* device_errors, void* stream) {
+  int rc = check_attention_args(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                num_heads, num_kv_heads, head_dim, block_size,
+                                max_blocks_per_seq, num_blocks, max_context_len, scale, q_dtype,
+                                kv_dtype, k_scale, v_scale);
+  if (rc != PKV_OK) return rc;
+  if (!group_start || !prefix_lens || num_groups < 0 || max_prefix_len < 0 ||
+      max_prefix_len > max_context_len)
+    return PKV_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PKV_OK;
+  if (kv_dtype != q_dtype || head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  pkv::AttnParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.num_seqs = num_seqs;
+  p.num_rows = num_seqs;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_heads / num_kv_heads;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.partition = kDefaultPartition;
+  p.max_parts = 2 * ((max_prefix_len + kCascadeChunk - 1) / kCascadeChunk) +
+                parts_for(max_context_len, kDefaultPartition);
+  if (p.max_parts > 16384) return PKV_ERR_UNSUPPORTED;
+  p.errors = device_errors;
+  p.q_scale = scale * pkv::kLog2e;
+  p.v_scale = 1.0f;
+  p.prefix_chunk = kCascadeChunk;
+  // pass 1: every member's query over its group's shared prefix (the prefill
+  // kernel, no causal mask, one partial per chunk of the prefix)
+  pkv::AttnParams pp = p;
+  pp.query_start_loc = group_start;
+  pp.num_seqs = num_groups;
+  pp.context_lens = prefix_lens;
+  pp.seq_rows = group_start;
+  pp.non_causal = 1;
+  pp.partial_out = 1;
+  // pass 2: each sequence over its own keys (the decode kernel), then the merge
+  pkv::AttnParams ps = p;
+  ps.prefix_lens = prefix_lens;
+  if (!pkv::tc_decode_supported(ps, q_dtype, kv_dtype, head_dim) ||
+      (num_groups > 0 && !pkv::tc_prefill_supported(pp, q_dtype, kv_dtype, head_dim)))
+    return PKV_ERR_UNSUPPORTED;
+  const size_t need =
+      pkv_cascade_workspace_size(num_seqs, num_heads, head_dim, max_context_len, max_prefix_len);
+  if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKV_ERR_INVALID_ARG;
+  const size_t heads = (size_t)num_seqs * num_heads * p.max_parts;
+  float* lse = static_cast<float*>(workspace);
+  float* o_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                           round_up(heads * sizeof(float), 256));
+  pp.lse = ps.lse = lse;
+  pp.o_part = ps.o_part = o_part;
+  if (num_groups > 0 && max_prefix_len > 0) {
+    rc = pkv::launch_prefill_tc(pp, q_dtype, num_seqs, st);
+    if (rc != PKV_OK) return rc;
+  }
+  rc = pkv::launch_paged_decode_tc(ps, q_dtype, kv_dtype, st);
+  if (rc != PKV_OK) return rc;
+  return pkv::launch_lse_merge(ps, q_dtype, head_dim, st);
 }
 
 int pkv_check_errors(uint32_t* device_errors, uint32_t* bits_out, void* stream) {

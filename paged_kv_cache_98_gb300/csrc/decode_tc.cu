@@ -54,6 +54,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "rows.cuh"
 #include "tc.cuh"
 
 namespace pkv {
@@ -136,7 +137,21 @@ struct Smem {
 
 struct Item {
   int seq, kvh, part, nparts, n, ntiles;
+  int kstart;  // first key of the sequence's own part (cascade decode: after its shared prefix)
+  int slot;    // partial slot of this partition
 };
+
+// Context of sequence s, clamped to the block table and the launched partitions.
+__device__ __forceinline__ int clamped_keys(const AttnParams& p, int s, bool report) {
+  const int cap_t = p.max_blocks_per_seq * kBlockSize, cap_l = p.max_parts * kPart;
+  const int cap = cap_t < cap_l ? cap_t : cap_l;
+  int keys = __ldg(p.context_lens + s);
+  if (keys < 0 || keys > cap) {
+    if (report) flag_error(p.errors, PKV_DEVERR_CONTEXT);
+    keys = keys < 0 ? 0 : cap;
+  }
+  return keys;
+}
 
 // Items are the non-empty (sequence, partition) pairs in sequence order, each
 // split over the KV heads (KV head fastest): item k has KV head k % Hkv and
@@ -162,6 +177,12 @@ __device__ __forceinline__ bool next_item(const AttnParams& p, const SM& sm, int
   it.nparts = (sm.seq_pack[lo + 1] >> kLenBits) - start;
   it.n = it.part == it.nparts - 1 ? (pk & ((1 << kLenBits) - 1)) + 1 : kPart;
   it.ntiles = (it.n + kTileKeys - 1) / kTileKeys;
+  it.kstart = 0;
+  it.slot = it.part;
+  if (p.prefix_lens != nullptr) {  // cascade decode: the keys after the shared prefix
+    it.kstart = cascade_prefix(p, lo, clamped_keys(p, lo, false), false);
+    it.slot += cascade_slots(p, it.kstart);
+  }
   return true;
 }
 
@@ -213,7 +234,8 @@ __global__ void __launch_bounds__(tc_threads(G16, FP8), 1)
   Smem<G16, FP8>& sm = *reinterpret_cast<Smem<G16, FP8>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool split = p.max_parts > 1;
+  // partials and a merge: several partitions, or cascade decode (prefix partials)
+  const bool split = p.max_parts > 1 || p.prefix_lens != nullptr;
   // kind::f16 (16-bit operands: 0 f16, 1 bf16) or kind::f8f6f4 (0 = E4M3)
   constexpr uint32_t kAB = (!FP8 && std::is_same<QT, BF16>::value) ? 1u : 0u;
   constexpr uint32_t kIdescS = tc::idesc_f16(kAB, 0, 0, 128, L::kSCols);
@@ -258,15 +280,10 @@ __global__ void __launch_bounds__(tc_threads(G16, FP8), 1)
   {
     const int S = p.num_rows, tid = threadIdx.x;
     const int chunk = (S + kThreads - 1) / kThreads;
-    const int cap_t = p.max_blocks_per_seq * kBlockSize, cap_l = p.max_parts * kPart;
-    const int cap = cap_t < cap_l ? cap_t : cap_l;
+    // keys of the sequence's own part (cascade decode: those after its shared prefix)
     auto keys_of = [&](int sq, bool report) {
-      int keys = __ldg(p.context_lens + sq);
-      if (keys < 0 || keys > cap) {
-        if (report) flag_error(p.errors, PKV_DEVERR_CONTEXT);
-        keys = keys < 0 ? 0 : cap;
-      }
-      return keys;
+      const int keys = clamped_keys(p, sq, report);
+      return keys - cascade_prefix(p, sq, keys, report);
     };
     int local = 0;
     for (int i = 0; i < chunk; ++i) {
@@ -330,7 +347,7 @@ __global__ void __launch_bounds__(tc_threads(G16, FP8), 1)
       int row = kv_rows;
       if (lane < nblk) {
         const int blk = __ldg(p.block_tables + (size_t)x.seq * p.max_blocks_per_seq +
-                              x.part * (kPart / kBlockSize) + lane);
+                              x.kstart / kBlockSize + x.part * (kPart / kBlockSize) + lane);
         if (blk >= 0 && blk < p.num_blocks)
           row = (blk * p.num_kv_heads + x.kvh) * kBlockSize;
         else if (!is_v && pi == 0)
@@ -536,7 +553,8 @@ __global__ void __launch_bounds__(tc_threads(G16, FP8), 1)
         v[i] = make_uint4(0, 0, 0, 0);
         if (key < x.n) {
           const int blk = __ldg(p.block_tables + (size_t)x.seq * p.max_blocks_per_seq +
-                                x.part * (kPart / kBlockSize) + key / kBlockSize);
+                                x.kstart / kBlockSize + x.part * (kPart / kBlockSize) +
+                                key / kBlockSize);
           if (blk >= 0 && blk < p.num_blocks) {
             const size_t row =
                 ((size_t)blk * p.num_kv_heads + x.kvh) * kBlockSize + (key & (kBlockSize - 1));
@@ -696,20 +714,21 @@ __global__ void __launch_bounds__(tc_threads(G16, FP8), 1)
       tc::tmem_wait_ld();
       tc::fence_before_sync();
       const int d = tid;
-      const bool direct = !split || x.nparts == 1;
+      // one partition and no shared prefix: straight to out
+      const bool direct = !split || (x.nparts == 1 && p.prefix_lens == nullptr);
       const size_t head0 = (size_t)x.seq * p.num_heads + (size_t)x.kvh * p.group;
       if (direct) {
         OutT* dst = static_cast<OutT*>(p.out) + head0 * kD + d;
 #pragma unroll
         for (int h = 0; h < L::kRows; ++h)
           if (h < p.group) store_out(dst + h * kD, o[h] * sm.stat_inv[b][h]);
-      } else {
-        float* dst = p.o_part + (head0 * p.max_parts + x.part) * kD + d;
+      } else if (x.slot < p.max_parts) {
+        float* dst = p.o_part + (head0 * p.max_parts + x.slot) * kD + d;
         const size_t stride = (size_t)p.max_parts * kD;
 #pragma unroll
         for (int h = 0; h < L::kRows; ++h)
           if (h < p.group) dst[h * stride] = o[h] * sm.stat_inv[b][h];
-        if (d < p.group) p.lse[(head0 + d) * p.max_parts + x.part] = sm.stat_lse[b][d];
+        if (d < p.group) p.lse[(head0 + d) * p.max_parts + x.slot] = sm.stat_lse[b][d];
       }
       return true;
     };
@@ -912,6 +931,7 @@ int launch_tc_typed(const AttnParams& p, cudaStream_t stream) {
     c.q = static_cast<const OutT*>(p.q) + head0 * kD;
     c.block_tables = p.block_tables + (size_t)r0 * p.max_blocks_per_seq;
     c.context_lens = p.context_lens + r0;
+    if (p.prefix_lens) c.prefix_lens = p.prefix_lens + r0;
     if (p.lse) {
       c.lse = p.lse + head0 * p.max_parts;
       c.o_part = p.o_part + head0 * p.max_parts * kD;

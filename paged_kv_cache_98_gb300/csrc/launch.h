@@ -34,6 +34,16 @@ struct AttnParams {
   float* o_part;                  // [rows][num_heads][max_parts][head_dim] (split only)
   float* lse;                     // [rows][num_heads][max_parts], base-2 units (split only)
   uint32_t* errors;               // device error word or nullptr
+  // Cascade decode (a prompt shared by a group of sequences is read once per
+  // group) and the prefill kernel's options for its shared-prefix pass.
+  // Zero / null for plain decode and prefill.
+  const int32_t* prefix_lens;     // decode, merge: [num_seqs] shared prefix tokens of each
+                                  // sequence (whole blocks); its partials come first
+  const int32_t* seq_rows;        // prefill: block-table and context_lens row of each
+                                  // sequence (null: the sequence itself)
+  int prefix_chunk;               // keys per partial of the shared-prefix pass (multiple of 512)
+  int non_causal;                 // prefill: every query sees all keys of its context
+  int partial_out;                // prefill: write (o, lse) partials, one slot per key chunk
 };
 
 int launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,

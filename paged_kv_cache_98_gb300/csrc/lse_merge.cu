@@ -6,7 +6,9 @@
 // max / sum of exponentials of "9、FlashAttention (4)".
 //
 // One CTA per (row, head), one thread per output element; the weights of all
-// partitions are computed once into shared memory.
+// partitions are computed once into shared memory.  In cascade decode the
+// partitions of a row are the chunks of its group's shared prefix followed by
+// those of its own keys.
 
 #include "common.cuh"
 #include "launch.h"
@@ -24,14 +26,21 @@ __global__ void __launch_bounds__(D) lse_merge_kernel(const AttnParams p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int seq;
   const int keys = row_keys(p, row, &seq);
-  const int np = (keys + p.partition - 1) / p.partition;
+  // cascade decode: the shared prefix's partials, then the sequence's own
+  const int pre = cascade_prefix(p, seq, keys, false);
+  int np = cascade_slots(p, pre) + (keys - pre + p.partition - 1) / p.partition;
+  if (np > p.max_parts) {  // a prefix longer than the launch was sized for
+    if (tid == 0) flag_error(p.errors, PKV_DEVERR_CONTEXT);
+    np = p.max_parts;
+  }
   const size_t head = (size_t)row * p.num_heads + h;
   OutT* out = static_cast<OutT*>(p.out) + head * D;
   if (np == 0) {
     store_out(out + tid, 0.0f);
     return;
   }
-  if (np == 1) return;  // the attention kernel wrote this row directly
+  // a single partition was written to out directly, except in cascade decode
+  if (np == 1 && p.prefix_lens == nullptr) return;
   const float* lse = p.lse + head * p.max_parts;
 
   float m = -INFINITY;

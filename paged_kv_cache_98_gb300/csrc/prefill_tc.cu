@@ -21,6 +21,21 @@
 // row's tile max exceeds it by more than 8 in base-2 units; the final
 // division by the row sum is exact.
 //
+// Shared-prefix mode (cascade decode): the "sequences" are groups of decode
+// sequences sharing a prompt, their query rows are the members' single
+// tokens, every query sees every key of the prompt (no causal mask), the
+// prompt's block-table and length row is the group's first member, items are
+// further split into 2048-key chunks, and each chunk writes normalised partial
+// outputs and their log-sum-exps (merged later with the members' own keys).
+// A group's members rarely fill more than one query tile, so in this mode both
+// warpgroups take the same query tile and alternate key tiles (even / odd),
+// each writing its own partial: the two softmaxes then overlap as they do for
+// two query tiles.  The second query buffer is then not needed: the query
+// tile sits in q[1] and q[0], right after the ring, becomes a fifth ring
+// stage; and V tiles trail K tiles by one (K0, K1, V0, K2, V1, ...), the order
+// the alternating MMAs take them in, so a V tile waiting for its softmax does
+// not hold back the next score tile's K.
+//
 // Warps: 0-3 softmax + epilogue of tile a, 4-7 of tile b, 8 TMEM owner + MMA
 // issuer, 9-11 TMA producers.  A K/V tile is 16 boxes of 16 rows x 128 B (one
 // per block and half); the boxes of each tile are spread over the three
@@ -46,7 +61,8 @@ constexpr int kProducers = 3;  // warps 9..11
 constexpr int kD = 128;
 constexpr int kTileKeys = 128;
 constexpr int kRowsM = 128;
-constexpr int kStages = 4;
+constexpr int kStages = 4;     // ring stages (5 in shared-prefix mode: q[0] joins the ring)
+constexpr int kMaxStages = 5;
 constexpr int kTileBytes = 128 * kD * 2;  // 32 KB: [2 halves][128 rows][128 B]
 constexpr int kHalf = kTileBytes / 2;
 constexpr int kTailBytes = kBlockSize * kD * 2;  // one block of V: [2 halves][16 rows][128 B]
@@ -58,15 +74,15 @@ constexpr int kBeyond = INT_MIN;  // block past the context (the box reads zeros
 
 struct Smem {
   alignas(1024) uint8_t ring[kStages][kTileBytes];
-  alignas(1024) uint8_t q[2][kTileBytes];
+  alignas(1024) uint8_t q[2][kTileBytes];  // must follow the ring (fifth stage)
   alignas(1024) uint8_t tail[kTailBytes];
   int seq_start[kMaxSeqs + 1];  // prefix of tile pairs per sequence
   int seq_qlen[kMaxSeqs];
   int seq_ctx[kMaxSeqs];
   int seq_q0[kMaxSeqs];
   int scan[kThreads / 32];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t q_full;
   uint64_t q_empty;
   uint64_t s_ready[2];  // per query tile
@@ -82,12 +98,26 @@ struct Smem {
 
 struct Item {
   int seq, kvh, ctx, q0;
+  int trow;          // block-table row of the sequence
   int t0[2], nt[2];  // first token (within the chunk) and tokens of tiles a, b (nt[1] = 0: none)
-  int pos0[2];       // absolute position of each tile's first token
-  int nkt[2];        // key tiles each query tile attends
-  int nk;            // key tiles of the item (max of the two)
+  int pos0[2];       // absolute position of each tile's first token (last key without mask)
+  int kt0;           // first key tile of the item (key chunks in shared-prefix mode)
+  int nkt[2];        // end (exclusive) of the key tiles each query tile attends in the item
+  int nk;            // end of the item's key tiles (max of the two)
+  int chunk;         // key chunk of the item (its partial slots)
+  int first[2];      // first key tile of each warpgroup in the item
+  int last[2];       // last key tile of each warpgroup (-1: none)
+  int step;          // key tiles between a warpgroup's tiles: 1, or 2 (shared-prefix mode)
   int tail_step;     // 16-key MMA step of the last key tile holding a partial block, else -1
 };
+
+// Key chunks of a sequence: all its key tiles in one item, or (shared-prefix
+// mode) prefix_chunk keys per item.
+__device__ __forceinline__ int key_chunks(const AttnParams& p, int ctx) {
+  if (p.prefix_chunk <= 0) return 1;
+  const int tiles = (ctx + kTileKeys - 1) / kTileKeys, per = p.prefix_chunk / kTileKeys;
+  return (tiles + per - 1) / per;
+}
 
 __device__ __forceinline__ bool next_item(const AttnParams& p, const Smem& sm, int& idx,
                                           int total, Item& it) {
@@ -101,27 +131,44 @@ __device__ __forceinline__ bool next_item(const AttnParams& p, const Smem& sm, i
     const int mid = (lo + hi + 1) >> 1;
     if (sm.seq_start[mid] <= pair) lo = mid; else hi = mid - 1;
   }
-  const int npairs = sm.seq_start[lo + 1] - sm.seq_start[lo];
-  const int mp = npairs - 1 - (pair - sm.seq_start[lo]);  // longest pairs first
-  const int rpt = kRowsM / p.group;                        // tokens per tile
+  const int rpt = kRowsM / p.group;  // tokens per tile
   const int qlen = sm.seq_qlen[lo];
   it.seq = lo;
   it.kvh = kvh;
   it.ctx = sm.seq_ctx[lo];
   it.q0 = sm.seq_q0[lo];
+  it.trow = p.seq_rows ? __ldg(p.seq_rows + lo) : lo;
+  const int nch = key_chunks(p, it.ctx);
+  const int npairs = (sm.seq_start[lo + 1] - sm.seq_start[lo]) / nch;
+  const int in_seq = pair - sm.seq_start[lo];
+  const int mp = npairs - 1 - in_seq / nch;  // longest pairs first
+  const bool alt = p.partial_out != 0;       // one query tile, alternating key tiles
+  it.chunk = in_seq % nch;
+  it.kt0 = p.prefix_chunk > 0 ? it.chunk * (p.prefix_chunk / kTileKeys) : 0;
+  const int kt1 = p.prefix_chunk > 0 ? it.kt0 + p.prefix_chunk / kTileKeys : INT_MAX;
   it.nk = 0;
 #pragma unroll
   for (int x = 0; x < 2; ++x) {
-    it.t0[x] = (2 * mp + x) * rpt;
+    it.t0[x] = (alt ? mp : 2 * mp + x) * rpt;
     it.nt[x] = max(0, min(rpt, qlen - it.t0[x]));
-    it.pos0[x] = it.ctx - qlen + it.t0[x];
-    it.nkt[x] = it.nt[x] > 0 ? (it.pos0[x] + it.nt[x] - 1) / kTileKeys + 1 : 0;
+    it.pos0[x] = p.non_causal ? it.ctx - 1 : it.ctx - qlen + it.t0[x];
+    const int last = p.non_causal ? it.pos0[x] : it.pos0[x] + it.nt[x] - 1;
+    it.nkt[x] = it.nt[x] > 0 ? min(kt1, last / kTileKeys + 1) : 0;
     it.nk = max(it.nk, it.nkt[x]);
   }
   const bool partial = (it.ctx & (kBlockSize - 1)) != 0;
   it.tail_step = partial && (it.ctx - 1) / kTileKeys == it.nk - 1
                      ? ((it.ctx - 1) % kTileKeys) / kBlockSize
                      : -1;
+  it.step = alt ? 2 : 1;
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    it.first[x] = it.kt0 + (alt ? x : 0);
+    const int end = alt ? it.nk : it.nkt[x];
+    it.last[x] = it.nt[x] > 0 && end > it.first[x]
+                     ? it.first[x] + (end - 1 - it.first[x]) / it.step * it.step
+                     : -1;
+  }
   return true;
 }
 
@@ -193,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- set-up ---------------------------------------------------------------------------
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(&sm.full[s], kProducers);
       mbar_init(&sm.empty[s], 1);
     }
@@ -232,18 +279,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (sq < S) {
         const int q0 = __ldg(p.query_start_loc + sq);
         int qlen = __ldg(p.query_start_loc + sq + 1) - q0;
-        int ctx = __ldg(p.context_lens + sq);
-        if (ctx < 0 || ctx > cap || qlen < 0 || qlen > ctx || q0 < 0 || q0 + qlen > p.num_rows) {
+        int ctx = __ldg(p.context_lens + (p.seq_rows ? __ldg(p.seq_rows + sq) : sq));
+        if (ctx < 0 || ctx > cap || qlen < 0 || (!p.non_causal && qlen > ctx) || q0 < 0 ||
+            q0 + qlen > p.num_rows) {
           flag_error(p.errors, PKV_DEVERR_CONTEXT);
           ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
-          qlen = qlen < 0 ? 0 : (qlen > ctx ? ctx : qlen);
+          qlen = qlen < 0 ? 0 : (!p.non_causal && qlen > ctx ? ctx : qlen);
           if (q0 < 0 || q0 + qlen > p.num_rows) qlen = 0;
         }
         sm.seq_qlen[sq] = qlen;
         sm.seq_ctx[sq] = ctx;
         sm.seq_q0[sq] = q0;
         const int tiles = (qlen * g + kRowsM - 1) / kRowsM;
-        local += (tiles + 1) / 2;
+        const int units = p.partial_out ? tiles : (tiles + 1) / 2;
+        local += ctx > 0 ? units * key_chunks(p, ctx) : 0;
       }
     }
     int incl = local;
@@ -261,7 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sq = tid * chunk + i;
       if (sq < S) {
         sm.seq_start[sq] = run;
-        run += ((sm.seq_qlen[sq] * g + kRowsM - 1) / kRowsM + 1) / 2;
+        const int c = sm.seq_ctx[sq];
+        const int tiles = (sm.seq_qlen[sq] * g + kRowsM - 1) / kRowsM;
+        run += c > 0 ? (p.partial_out ? tiles : (tiles + 1) / 2) * key_chunks(p, c) : 0;
       }
     }
     if (tid == kThreads - 1) sm.seq_start[S] = base + incl;
@@ -279,6 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pw = warp - 9;
     const int mine = (8 - pw + kProducers - 1) / kProducers;  // blocks per tile: 3, 3, 2
     const bool my_lane = (lane & 7) % kProducers == pw;
+    const bool alt = p.partial_out != 0;  // shared-prefix mode
+    const int nst = alt ? kMaxStages : kStages;
+    uint8_t* const ring = &sm.ring[0][0];  // stage 4 (shared-prefix mode) is q[0]
     int idx = blockIdx.x;
     uint32_t pos = 0;
     int nitem = 0, ntail = 0;
@@ -289,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto fetch = [&](int c) -> int {
       const int b = 32 * c + lane;
       return b < (x.ctx + kBlockSize - 1) / kBlockSize
-                 ? __ldg(p.block_tables + (size_t)x.seq * p.max_blocks_per_seq + b)
+                 ? __ldg(p.block_tables + (size_t)x.trow * p.max_blocks_per_seq + b)
                  : kBeyond;
     };
     auto to_row = [&](int blk) -> int {
@@ -299,15 +353,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       return kv_rows;
     };
     auto issue = [&](int t, int row, bool is_v) -> bool {
-      const int st = pos % kStages;
+      const int st = pos % nst;
       bool good = true;
       if (lane == 0) {
-        if (pos >= kStages) good = wait_bar(&sm.empty[st], ((pos / kStages) - 1) & 1, abort);
+        if (pos >= (uint32_t)nst) good = wait_bar(&sm.empty[st], ((pos / nst) - 1) & 1, abort);
         if (good) mbar_arrive_expect_tx(&sm.full[st], mine * (kTileBytes / 8));
       }
       if (!__shfl_sync(kFull, (int)good, 0)) return false;
       if ((lane >> 3) == (t & 3) && my_lane) {
-        uint8_t* dst = &sm.ring[st][0] + (lane & 7) * (kBlockSize * 128);
+        uint8_t* dst = ring + (size_t)st * kTileBytes + (lane & 7) * (kBlockSize * 128);
         const CUtensorMap* map = is_v ? &tm_v : &tm_k;
         tc::tma_load_2d(dst, map, 0, row, &sm.full[st]);
         tc::tma_load_2d(dst + kHalf, map, 64, row, &sm.full[st]);
@@ -323,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && ntail >= 1) good = wait_bar(&sm.tail_free, (ntail - 1) & 1, abort);
       if (!__shfl_sync(kFull, (int)good, 0)) return false;
       const int bi = (x.ctx - 1) / kBlockSize;
-      const int blk = __ldg(p.block_tables + (size_t)x.seq * p.max_blocks_per_seq + bi);
+      const int blk = __ldg(p.block_tables + (size_t)x.trow * p.max_blocks_per_seq + bi);
       const bool bok = blk >= 0 && blk < p.num_blocks;
       const uint8_t* src =
           p.v_cache + ((size_t)(bok ? blk : 0) * p.num_kv_heads + x.kvh) * kBlockSize * (kD * 2);
@@ -348,39 +402,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (pw == 0 && lane == 0) {
         if (nitem >= 1) good = wait_bar(&sm.q_empty, (nitem - 1) & 1, abort);
         if (good) {
-          const bool hb = x.nt[1] > 0;
-          mbar_arrive_expect_tx(&sm.q_full, (hb ? 2 : 1) * kTileBytes);
-          for (int qt = 0; qt < (hb ? 2 : 1); ++qt) {
+          // shared-prefix mode: one query tile, in q[1]
+          const int nq = alt ? 1 : (x.nt[1] > 0 ? 2 : 1);
+          mbar_arrive_expect_tx(&sm.q_full, nq * kTileBytes);
+          for (int qt = 0; qt < nq; ++qt) {
+            uint8_t* dq = &sm.q[alt ? 1 : qt][0];
             const int tok = x.q0 + x.t0[qt];
-            tc::tma_load_3d(&sm.q[qt][0], &tm_q, 0, x.kvh * g, tok, &sm.q_full);
-            tc::tma_load_3d(&sm.q[qt][kHalf], &tm_q, 64, x.kvh * g, tok, &sm.q_full);
+            tc::tma_load_3d(dq, &tm_q, 0, x.kvh * g, tok, &sm.q_full);
+            tc::tma_load_3d(dq + kHalf, &tm_q, 64, x.kvh * g, tok, &sm.q_full);
           }
         }
       }
       ok = __shfl_sync(kFull, (int)good, 0) != 0;
-      int raw_next = x.nk > 4 ? fetch(1) : kBeyond;
-      int row = to_row(fetch(0));
-      for (int t = 0; ok && t < x.nk; ++t) {
-        if (t > 0 && (t & 3) == 0) {  // next 32 blocks
-          row = to_row(raw_next);
-          raw_next = t + 4 < x.nk ? fetch((t >> 2) + 1) : kBeyond;
+      // Block rows of the 32-block table chunks (4 key tiles each) the tiles
+      // being issued fall in: two chunks cached (K runs a tile ahead of V in
+      // shared-prefix mode), the next one read ahead.
+      int rc_c[2] = {-1, -1}, rc_row[2] = {kv_rows, kv_rows};
+      int pre_c = x.kt0 >> 2, pre_raw = fetch(pre_c);
+      auto row_for = [&](int t) -> int {
+        const int c = t >> 2;
+        if (rc_c[0] == c) return rc_row[0];
+        if (rc_c[1] == c) return rc_row[1];
+        const int r = to_row(pre_c == c ? pre_raw : fetch(c));
+        const int sl = rc_c[0] < rc_c[1] ? 0 : 1;  // replace the older chunk
+        rc_c[sl] = c;
+        rc_row[sl] = r;
+        pre_c = c + 1;
+        pre_raw = 4 * pre_c < x.nk ? fetch(pre_c) : kBeyond;
+        return r;
+      };
+      if (!alt) {
+        for (int t = x.kt0; ok && t < x.nk; ++t) {
+          ok = issue(t, row_for(t), false);
+          if (ok && pw == 0 && t == x.nk - 1 && x.tail_step >= 0) ok = load_tail();
+          if (ok) ok = issue(t, row_for(t), true);
         }
-        ok = issue(t, row, false);
-        if (ok && pw == 0 && t == x.nk - 1 && x.tail_step >= 0) ok = load_tail();
-        if (ok) ok = issue(t, row, true);
+      } else {
+        // K0, K1, V0, K2, V1, ...
+        ok = issue(x.kt0, row_for(x.kt0), false);
+        for (int t = x.kt0; ok && t < x.nk; ++t) {
+          if (t + 1 < x.nk) ok = issue(t + 1, row_for(t + 1), false);
+          if (ok && pw == 0 && t == x.nk - 1 && x.tail_step >= 0) ok = load_tail();
+          if (ok) ok = issue(t, row_for(t), true);
+        }
       }
       ++nitem;
     }
     if (!ok && lane == 0) {
       flag_error(p.errors, PKV_DEVERR_TIMEOUT);
-      for (uint32_t y = pos > kStages ? pos - kStages : 0; y < pos; ++y)
-        mbar_wait(&sm.full[y % kStages], (y / kStages) & 1, 10000000ull);
+      for (uint32_t y = pos > (uint32_t)nst ? pos - nst : 0; y < pos; ++y)
+        mbar_wait(&sm.full[y % nst], (y / nst) & 1, 10000000ull);
     }
   } else if (warp == 8) {
     // ---- MMA issuer --------------------------------------------------------------------
     // Order per item: S_a(0), S_b(0), then for each key tile t:
     //   P_a(t) V_t, S_a(t+1), P_b(t) V_t, S_b(t+1)
     // so each softmax warpgroup works while the tensor pipe serves the other.
+    // Shared-prefix mode (warpgroup a even tiles, b odd): S_a(0), S_b(1), then
+    //   P_a(t) V_t, S_a(t+2), P_b(t+1) V_t+1, S_b(t+3)   for t = 0, 2, ...
     if (lane == 0) {
       int idx = blockIdx.x;
       uint32_t pos = 0;
@@ -391,16 +470,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       Item x;
       const uint32_t qaddr[2] = {smem_u32(&sm.q[0][0]), smem_u32(&sm.q[1][0])};
       const uint32_t taddr = smem_u32(&sm.tail[0]);
+      const bool alt = p.partial_out != 0;  // shared-prefix mode
+      const int nst = alt ? kMaxStages : kStages;
       auto acquire = [&](int& st) -> bool {
-        st = pos % kStages;
-        const bool r = wait_bar(&sm.full[st], (pos / kStages) & 1, abort);
+        st = pos % nst;
+        const bool r = wait_bar(&sm.full[st], (pos / nst) & 1, abort);
         ++pos;
         if (r) tc::fence_after_sync();
         return r;
       };
       // Operand descriptors are built once; a step moves the start address
       // field (bytes / 16 in the low bits, no carry below 256 KB).
-      const uint64_t dq[2] = {tc::smem_desc(qaddr[0], 16, 1024, tc::kLayoutSw128),
+      // (shared-prefix mode: both warpgroups' scores from the query tile in q[1])
+      const uint64_t dq[2] = {tc::smem_desc(qaddr[alt ? 1 : 0], 16, 1024, tc::kLayoutSw128),
                               tc::smem_desc(qaddr[1], 16, 1024, tc::kLayoutSw128)};
       const uint64_t dk0 = tc::smem_desc(smem_u32(&sm.ring[0][0]), 16, 1024, tc::kLayoutSw128);
       const uint64_t dv0 =
@@ -420,7 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto mma_pv = [&](int qt, int st, int t) -> bool {
         if (!wait_bar(&sm.p_ready[qt], np[qt] & 1, abort)) return false;
         ++np[qt];
-        if (t == 0 && nit[qt] >= 1 && !wait_bar(&sm.o_free[qt], (nit[qt] - 1) & 1, abort))
+        if (t == x.first[qt] && nit[qt] >= 1 &&
+            !wait_bar(&sm.o_free[qt], (nit[qt] - 1) & 1, abort))
           return false;  // the previous item's O has been read out
         tc::fence_after_sync();
         const uint64_t dv = dv0 + (uint64_t)(st * (kTileBytes >> 4));
@@ -429,49 +512,86 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kTileKeys / 16; ++kk) {
           const uint64_t b = kk == ts ? dtail : dv + (uint64_t)((kk * (kBlockSize * 128)) >> 4);
-          mma_f16_tmem_a(d, a + kk * 8, b, kIdescO, (t | kk) != 0);
+          mma_f16_tmem_a(d, a + kk * 8, b, kIdescO, (t != x.first[qt]) || kk != 0);
         }
-        if (t == x.nkt[qt] - 1) tc::mma_commit(&sm.o_done[qt]);
+        if (t == x.last[qt]) tc::mma_commit(&sm.o_done[qt]);
+        return true;
+      };
+      // K(t) into S of warpgroup qt, its stage released, and Q released after
+      // the item's last S
+      auto s_tile = [&](int qt, int t) -> bool {
+        int st = 0;
+        if (!acquire(st)) return false;
+        mma_s(qt, st);
+        tc::mma_commit(&sm.empty[st]);
+        if (t == x.nk - 1) tc::mma_commit(&sm.q_empty);
+        return true;
+      };
+      auto tail_wait = [&](int t) -> bool {
+        if (t != x.nk - 1 || x.tail_step < 0) return true;
+        const bool r = wait_bar(&sm.tail_full, ntail & 1, abort);
+        if (r) tc::fence_after_sync();
+        return r;
+      };
+      // shared-prefix mode: the two warpgroups on alternate key tiles; the
+      // ring holds K0, K1, V0, K2, V1, K3, ... in the order taken here
+      auto alternate = [&]() -> bool {
+        int va = 0, vb = 0;
+        const bool hb = x.last[1] >= 0;
+        if (!s_tile(0, x.kt0)) return false;
+        if (hb && !s_tile(1, x.kt0 + 1)) return false;
+        for (int t = x.kt0; t < x.nk; t += 2) {
+          if (!(acquire(va) && tail_wait(t) && mma_pv(0, va, t))) return false;
+          tc::mma_commit(&sm.empty[va]);
+          if (t + 2 < x.nk && !s_tile(0, t + 2)) return false;
+          if (t + 1 < x.nk) {
+            if (!(acquire(vb) && tail_wait(t + 1) && mma_pv(1, vb, t + 1))) return false;
+            tc::mma_commit(&sm.empty[vb]);
+            if (t + 3 < x.nk && !s_tile(1, t + 3)) return false;
+          }
+        }
         return true;
       };
       while (ok && next_item(p, sm, idx, total, x)) {
-        const bool hb = x.nt[1] > 0;
+        const bool ha = x.last[0] >= 0;
+        const bool hb = x.last[1] >= 0;
         int kst = 0, vst = 0;
         ok = wait_bar(&sm.q_full, nitem & 1, abort);
         if (ok) tc::fence_after_sync();
-        if (ok) ok = acquire(kst);
-        if (ok) {
-          mma_s(0, kst);
-          if (hb) mma_s(1, kst);
-          tc::mma_commit(&sm.empty[kst]);
-          if (x.nk == 1) tc::mma_commit(&sm.q_empty);
-        }
-        for (int t = 0; ok && t < x.nk; ++t) {
-          const bool more = t + 1 < x.nk;
-          ok = acquire(vst);
-          if (ok && t == x.nk - 1 && x.tail_step >= 0) {
-            ok = wait_bar(&sm.tail_full, ntail & 1, abort);
-            if (ok) tc::fence_after_sync();
-          }
-          if (ok && t < x.nkt[0]) ok = mma_pv(0, vst, t);
-          if (ok && more) {
-            ok = acquire(kst);
-            if (ok && t + 1 < x.nkt[0]) mma_s(0, kst);
-          }
-          if (ok && hb) ok = mma_pv(1, vst, t);
-          if (!ok) break;
-          tc::mma_commit(&sm.empty[vst]);
-          if (more) {
+        if (ok && x.step == 2) {
+          ok = alternate();
+        } else if (ok) {
+          ok = acquire(kst);
+          if (ok) {
+            if (ha) mma_s(0, kst);
             if (hb) mma_s(1, kst);
             tc::mma_commit(&sm.empty[kst]);
-            if (t + 1 == x.nk - 1) tc::mma_commit(&sm.q_empty);
+            if (x.nk - x.kt0 == 1) tc::mma_commit(&sm.q_empty);
+          }
+          for (int t = x.kt0; ok && t < x.nk; ++t) {
+            const bool more = t + 1 < x.nk;
+            ok = acquire(vst);
+            if (ok) ok = tail_wait(t);
+            if (ok && t <= x.last[0]) ok = mma_pv(0, vst, t);
+            if (ok && more) {
+              ok = acquire(kst);
+              if (ok && t + 1 <= x.last[0]) mma_s(0, kst);
+            }
+            if (ok && hb) ok = mma_pv(1, vst, t);
+            if (!ok) break;
+            tc::mma_commit(&sm.empty[vst]);
+            if (more) {
+              if (hb) mma_s(1, kst);
+              tc::mma_commit(&sm.empty[kst]);
+              if (t + 1 == x.nk - 1) tc::mma_commit(&sm.q_empty);
+            }
           }
         }
         if (ok && x.tail_step >= 0) {
           tc::mma_commit(&sm.tail_free);
           ++ntail;
         }
-        ++nit[0];
+        if (ha) ++nit[0];
         if (hb) ++nit[1];
         ++nitem;
       }
@@ -498,17 +618,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     Item x;
     while (ok && next_item(p, sm, idx, total, x)) {
-      if (x.nt[qt] == 0) continue;  // no tile b in this item
-      const int tok = tid / g;      // token within the tile
+      const int tok = tid / g;  // token within the tile
       // rows past the tile's tokens compute on whatever Q holds there; their
       // output is never stored
       const bool valid = tid < x.nt[qt] * g;
-      const int qpos = x.pos0[qt] + tok;
+      // shared-prefix mode: the warpgroup's partial slot of this key chunk
+      const size_t head = (size_t)(x.q0 + x.t0[qt] + tok) * p.num_heads + (size_t)x.kvh * g + tid % g;
+      const int slot = 2 * x.chunk + qt;
+      if (x.last[qt] < 0) {
+        // no key tile for this warpgroup here (no tile b, or a one-tile chunk in
+        // shared-prefix mode, whose empty partial then weighs nothing)
+        if (p.partial_out && valid && x.nt[qt] > 0 && slot < p.max_parts) {
+          p.lse[head * p.max_parts + slot] = -INFINITY;
+          float4* z = reinterpret_cast<float4*>(p.o_part + (head * p.max_parts + slot) * kD);
+#pragma unroll 4
+          for (int i = 0; i < kD / 4; ++i) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        continue;
+      }
+      const int qpos = x.pos0[qt] + (p.non_causal ? 0 : tok);
       float m_run = -INFINITY;
       float l8[8];  // partial row sums (independent chains)
 #pragma unroll
       for (int i = 0; i < 8; ++i) l8[i] = 0.0f;
-      for (int t = 0; t < x.nkt[qt]; ++t, ++ns) {
+      for (int t = x.first[qt]; t <= x.last[qt]; t += x.step, ++ns) {
         ok = all_group(wait_bar(&sm.s_ready[qt], ns & 1, abort), qt);
         if (!ok) break;
         tc::fence_after_sync();
@@ -543,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool need = mt > m_run + kRescaleAt;
         float alpha = 1.0f;
         if (need) {
-          alpha = (t == 0) ? 0.0f : fast_exp2(m_run - mt);
+          alpha = (t == x.first[qt]) ? 0.0f : fast_exp2(m_run - mt);
           m_run = mt;
 #pragma unroll
           for (int i = 0; i < 8; ++i) l8[i] *= alpha;
@@ -564,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_st16(s_col + 16 * h, pk);
         }
         // the product of tile t adds onto O: rescale it first when a row's max moved
-        if (t > 0 && __any_sync(kFull, need)) {
+        if (t > x.first[qt] && __any_sync(kFull, need)) {
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             float ov[32];
@@ -587,15 +720,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_after_sync();
       const float l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
       const float inv = valid ? 1.0f / l : 0.0f;
-      OutT* orow = static_cast<OutT*>(p.out) +
-                   ((size_t)(x.q0 + x.t0[qt] + tok) * p.num_heads + (size_t)x.kvh * g + tid % g) *
-                       kD;
+      OutT* orow = static_cast<OutT*>(p.out) + head * kD;
+      // shared-prefix mode: the normalised partial and its log-sum-exp (base 2,
+      // scaled units), in the warpgroup's slot of the chunk
+      const bool part = p.partial_out && slot < p.max_parts;
+      float* prow = part ? p.o_part + (head * p.max_parts + slot) * kD : nullptr;
+      if (part && valid) p.lse[head * p.max_parts + slot] = m_run + log2f(l);
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float ov[32];
         tc::tmem_ld32(o_col + 32 * c, ov);
         tc::tmem_wait_ld();
-        if (valid) {
+        if (part) {
+          if (valid) {
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              reinterpret_cast<float4*>(prow + 32 * c)[q4] =
+                  make_float4(ov[q4 * 4] * inv, ov[q4 * 4 + 1] * inv, ov[q4 * 4 + 2] * inv,
+                              ov[q4 * 4 + 3] * inv);
+          }
+        } else if (valid) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint4 w;
@@ -638,6 +782,8 @@ int launch_typed(const AttnParams& p, int total_q, cudaStream_t stream) {
   static_assert(offsetof(Smem, ring) % 1024 == 0 && offsetof(Smem, q) % 1024 == 0 &&
                     offsetof(Smem, tail) % 1024 == 0,
                 "swizzled buffers must start on 1024-byte boundaries");
+  static_assert(offsetof(Smem, q) == offsetof(Smem, ring) + kStages * kTileBytes,
+                "q[0] is the ring's fifth stage in shared-prefix mode");
   auto kern = prefill_tc_kernel<QT>;
   static bool configured = false;
   if (!configured) {
@@ -651,7 +797,8 @@ int launch_typed(const AttnParams& p, int total_q, cudaStream_t stream) {
                           kRowsM;
   const long long items = (tiles + p.num_seqs) / 2 * p.num_kv_heads;
   int grid = sm_count();
-  if (items < grid) grid = (int)(items > 0 ? items : 1);
+  // (key chunks multiply the items of the shared-prefix pass)
+  if (!p.partial_out && items < grid) grid = (int)(items > 0 ? items : 1);
   kern<<<grid, kThreads, smem, stream>>>(p, tk, tv, tq, (int)kv_rows);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

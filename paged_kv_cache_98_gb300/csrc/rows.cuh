@@ -37,4 +37,24 @@ __device__ __forceinline__ int row_keys(const AttnParams& p, int row, int* seq_o
   return keys;
 }
 
+// Cascade decode: first key of sequence s's own part (its shared prefix), for a
+// context of `keys` tokens.  The prefix must be whole blocks within the
+// context; otherwise it is cut back to one and the error flagged.
+__device__ __forceinline__ int cascade_prefix(const AttnParams& p, int s, int keys, bool report) {
+  if (p.prefix_lens == nullptr) return 0;
+  int pre = __ldg(p.prefix_lens + s);
+  if (pre < 0 || pre > keys || (pre & (kBlockSize - 1)) != 0) {
+    if (report) flag_error(p.errors, PKV_DEVERR_CONTEXT);
+    pre = pre < 0 ? 0 : (pre > keys ? keys : pre);
+    pre &= ~(kBlockSize - 1);
+  }
+  return pre;
+}
+
+// Partial slots of the shared-prefix pass that precede sequence s's own: two
+// per chunk of the prefix (its even and its odd key tiles).
+__device__ __forceinline__ int cascade_slots(const AttnParams& p, int prefix) {
+  return p.prefix_chunk > 0 ? 2 * ((prefix + p.prefix_chunk - 1) / p.prefix_chunk) : 0;
+}
+
 }  // namespace pkv

@@ -111,3 +111,39 @@ def test_prefill_argument_validation(lib):
     args = [256, 256, 512, 512, 1024, 2048, None, 1, 10, 10, 8, 2, 128, 16, 4, 8, 64, 0.1, 1, 1,
             1.0, 1.0, None, 0, None, None]
     assert f(*args) == -1  # query_start_loc missing
+
+
+def _cascade(lib, **over):
+    a = dict(out=256, q=256, k_cache=512, v_cache=512, block_tables=1024, context_lens=2048,
+             group_start=4096, prefix_lens=8192, num_seqs=2, num_groups=1, num_heads=8,
+             num_kv_heads=2, head_dim=128, block_size=16, max_blocks_per_seq=4, num_blocks=8,
+             max_context_len=64, max_prefix_len=32, scale=0.1, q_dtype=1, kv_dtype=1,
+             k_scale=1.0, v_scale=1.0, workspace=None, workspace_bytes=0, device_errors=None,
+             stream=None)
+    a.update(over)
+    return lib.pkv_paged_attention_decode_cascade(*a.values())
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(group_start=None), -1),
+    (dict(prefix_lens=None), -1),
+    (dict(max_prefix_len=128), -1),   # longer than max_context_len
+    (dict(num_groups=-1), -1),
+    (dict(head_dim=96), -2),
+    (dict(head_dim=64), -2),          # the cascade runs on the 128-dim tensor-core kernels
+    (dict(kv_dtype=2), -2),           # 16-bit caches only
+    (dict(q=None), -1),
+    (dict(num_seqs=0), 0),
+])
+def test_cascade_argument_validation(lib, over, status):
+    assert _cascade(lib, **over) == status
+
+
+def test_cascade_workspace_size(lib):
+    # two partials per 2048-key chunk of the prefix, then 512-token partitions
+    slots = 2 * 3 + 8
+    heads = 64 * 32 * slots
+    want = (-(-heads * 4 // 256) * 256) + (-(-heads * 128 * 4 // 256) * 256)
+    assert pkv.cascade_workspace_size(64, 32, 128, 4096, 5000) == want
+    # always a workspace, even for one partition and no prefix
+    assert pkv.cascade_workspace_size(1, 8, 128, 16, 0) > 0

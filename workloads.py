@@ -86,6 +86,37 @@ class Workload:
     def prefill_ids(self) -> np.ndarray:
         return np.nonzero(self.q_lens > 1)[0]
 
+    def cascade_groups(self):
+        """Cascade-decode grouping of the decode sequences (in decode_ids
+        order): (group_start [G + 1] int32, prefix_lens [S] int32).  Consecutive
+        members of one sharing group form a group whose prefix is their common
+        leading blocks (whole blocks within every member's context); runs of
+        other sequences form groups with no shared prefix."""
+        ids = [int(s) for s in self.decode_ids()]
+        group_of = {s: gi for gi, g in enumerate(self.shared_groups) for s in g}
+        starts, prefix = [0], np.zeros(len(ids), np.int32)
+        i = 0
+        while i < len(ids):
+            gi = group_of.get(ids[i])
+            j = i + 1
+            if gi is not None:
+                while j < len(ids) and group_of.get(ids[j]) == gi:
+                    j += 1
+            k = 0
+            if j - i > 1:
+                tabs = [self.block_tables[s] for s in ids[i:j]]
+                n = min(int(self.context_lens[s]) for s in ids[i:j]) // BLOCK_SIZE
+                while k < n and all(t[k] == tabs[0][k] for t in tabs):
+                    k += 1
+            if k == 0:  # nothing shared: extend the run of unshared sequences
+                while j < len(ids) and (group_of.get(ids[j]) is None or
+                                        len(self.shared_groups[group_of[ids[j]]]) < 2):
+                    j += 1
+            prefix[i:j] = k * BLOCK_SIZE
+            starts.append(j)
+            i = j
+        return np.asarray(starts, np.int32), prefix
+
     def kv_read_bytes(self, ids=None) -> int:
         """Bytes of K and V one decode pass reads: every context token, once per KV head."""
         ids = self.decode_ids() if ids is None else ids
