@@ -225,6 +225,39 @@ class GpuStep:
         if pkv.check_errors(self.err) != 0:
             raise RuntimeError("device-side checks failed while filling the cache")
 
+    def cascade_timed(self, steps: int, warmup: int) -> float:
+        """Mean CUDA-event time (ms) of the decode through the cascade entry
+        point; its output is checked against the plain decode's."""
+        import torch
+        gs, pre = self.w.cascade_groups()
+        gs_d = torch.from_numpy(gs).to(self.dev)
+        pre_d = torch.from_numpy(pre).to(self.dev)
+        S, H, D = self.q_dec.shape
+        mp = int(pre.max()) if len(pre) else 0
+        ws = torch.empty(max(256, self.pkv.cascade_workspace_size(S, H, D, self.max_ctx, mp)),
+                         dtype=torch.uint8, device=self.dev)
+        out = torch.empty_like(self.out)
+
+        def one():
+            self.pkv.paged_attention_decode_cascade(
+                out, self.q_dec, self.kc, self.vc, self.bt, self.cl, gs_d, pre_d, self.w.scale,
+                max_context_len=self.max_ctx, max_prefix_len=mp, workspace=ws,
+                device_errors=self.err)
+        for _ in range(warmup):
+            one()
+        self.decode()
+        torch.cuda.synchronize(self.dev)
+        if (out.float() - self.out.float()).abs().max().item() > 0.05:
+            raise RuntimeError("cascade decode disagrees with plain decode")
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(steps):
+            one()
+        t1.record()
+        torch.cuda.synchronize(self.dev)
+        return t0.elapsed_time(t1) / steps
+
     def launches_per_step(self) -> int:
         n = 1  # cache write
         if len(self.dec):
@@ -535,6 +568,13 @@ def other_workloads(dev, peak, barrier):
             ub = unique_kv_bytes(w)
             d["kv_bytes_unique"] = ub
             d["decode_GBps_unique"] = round(ub / (res["decode_ms"] * 1e-3) / 1e9, 1)
+            # the same decode through the cascade entry point (each shared prompt
+            # block read once per group of samples)
+            cms = st.cascade_timed(steps, 5)
+            d["cascade_decode_ms"] = round(cms, 5)
+            d["cascade_GBps_logical"] = round(kvb / (cms * 1e-3) / 1e9, 1)
+            d["cascade_GBps_unique"] = round(ub / (cms * 1e-3) / 1e9, 1)
+            d["cascade_speedup"] = round(res["decode_ms"] / cms, 3)
         if len(w.prefill_ids()):
             flops = 0
             for s in w.prefill_ids():
