@@ -106,6 +106,8 @@ def _declare(L):
         [_P] * 6 + [_I] * 7 + [_D, _I, _I, _D, _D, _I])
     L.orc_paged_attention_prefill.restype = _I
     L.orc_paged_attention_prefill.argtypes = [_P] * 7 + [_I] * 8 + [_D, _I, _I, _D, _D]
+    L.orc_paged_attention_prefill_tree.restype = _I
+    L.orc_paged_attention_prefill_tree.argtypes = [_P] * 8 + [_I] * 8 + [_D, _I, _I, _D, _D]
 
 
 def _ptr(a: np.ndarray | None):
@@ -259,6 +261,26 @@ def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, num_
     else:
         rc = lib().orc_paged_attention_decode(*args)
     _check(rc, "orc_paged_attention_decode")
+    return out
+
+
+def paged_attention_prefill_tree(q, k_cache, v_cache, block_tables, context_lens,
+                                 query_start_loc, tree_mask, num_kv_heads, head_dim, block_size,
+                                 num_blocks, scale, q_dtype, kv_dtype, k_scale=1.0,
+                                 v_scale=1.0) -> np.ndarray:
+    """Tree-masked chunk attention: tree_mask[row] bit j = the chunk key j is
+    visible to that query (see orc_paged_attention_prefill_tree)."""
+    TQ, H, D = q.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    tm = np.ascontiguousarray(tree_mask, dtype=np.uint64)
+    out = np.empty((TQ, H, D), dtype=np.float64)
+    rc = lib().orc_paged_attention_prefill_tree(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), _ptr(cl), _ptr(qsl),
+        _ptr(tm), len(cl), TQ, H, num_kv_heads, D, block_size, bt.shape[1], num_blocks, scale,
+        q_dtype, kv_dtype, k_scale, v_scale)
+    _check(rc, "orc_paged_attention_prefill_tree")
     return out
 
 

@@ -238,6 +238,50 @@ int attend_row(double* out, const double* q, const int32_t* table, int n_keys,
   return 0;
 }
 
+// The same definition over an explicit set of key positions of the sequence
+// (ascending): used for tree-masked chunks, where a query sees the prior
+// context and only some of the chunk's own keys.
+int attend_keys(double* out, const double* q, const int32_t* table, const std::vector<int>& keys,
+                const uint8_t* k_cache, const uint8_t* v_cache, int kv_head, int num_kv_heads,
+                int head_dim, int block_size, int num_blocks, double scale, int kv_dtype,
+                double k_scale, double v_scale) {
+  for (int d = 0; d < head_dim; ++d) out[d] = 0.0;
+  const int n = (int)keys.size();
+  if (n == 0) return 0;
+  const bool fp8 = kv_dtype == ORC_E4M3;
+  std::vector<double> z(n);
+  for (int i = 0; i < n; ++i) {
+    const int t = keys[i];
+    int blk = table[t / block_size];
+    if (blk < 0 || blk >= num_blocks) return -1;
+    size_t row = ((size_t)blk * num_kv_heads + kv_head) * block_size + t % block_size;
+    double acc = 0.0;
+    for (int d = 0; d < head_dim; ++d) {
+      double kd = decode_elem(k_cache, row * head_dim + d, kv_dtype);
+      if (fp8) kd *= k_scale;
+      acc += q[d] * kd;
+    }
+    z[i] = scale * acc;
+  }
+  double m = z[0];
+  for (int i = 1; i < n; ++i) m = z[i] > m ? z[i] : m;
+  double l = 0.0;
+  for (int i = 0; i < n; ++i) {
+    const int t = keys[i];
+    double w = std::exp(z[i] - m);
+    l += w;
+    int blk = table[t / block_size];
+    size_t row = ((size_t)blk * num_kv_heads + kv_head) * block_size + t % block_size;
+    for (int d = 0; d < head_dim; ++d) {
+      double vd = decode_elem(v_cache, row * head_dim + d, kv_dtype);
+      if (fp8) vd *= v_scale;
+      out[d] += w * vd;
+    }
+  }
+  for (int d = 0; d < head_dim; ++d) out[d] /= l;
+  return 0;
+}
+
 bool dtype_ok(int dt) { return dt == ORC_F16 || dt == ORC_BF16 || dt == ORC_E4M3; }
 
 }  // namespace
@@ -562,6 +606,54 @@ int orc_paged_attention_prefill(double* out, const void* q, const uint8_t* k_cac
         if (attend_row(out + row * head_dim, qrow.data(), table, pos + 1, k_cache, v_cache,
                        h / group, num_kv_heads, head_dim, block_size, num_blocks, scale,
                        kv_dtype, k_scale, v_scale, nullptr))
+          return -2;
+      }
+    }
+  }
+  return 0;
+}
+
+// Tree-masked chunk attention, for verifying a tree of draft tokens
+// ([P2] "MEDUSA推理框架", "Tree Attention": candidate tokens of several heads
+// form a tree verified in one pass under an attention mask; "EAGLE2推理",
+// "重排阶段": the mask is adjusted so that each token sees only its
+// ancestors).  Sequence s's chunk holds q_len <= 64 draft tokens at positions
+// base = ctx - q_len .. ctx - 1; query i sees every key before base, and the
+// chunk key base + j when bit j of tree_mask[q0 + i] is set (its ancestors
+// and itself).  A mask with bits 0..i for every i is ordinary causal prefill.
+int orc_paged_attention_prefill_tree(double* out, const void* q, const uint8_t* k_cache,
+                                     const uint8_t* v_cache, const int32_t* block_tables,
+                                     const int32_t* context_lens, const int32_t* query_start_loc,
+                                     const uint64_t* tree_mask, int num_seqs, int total_q,
+                                     int num_heads, int num_kv_heads, int head_dim,
+                                     int block_size, int max_blocks_per_seq, int num_blocks,
+                                     double scale, int q_dtype, int kv_dtype, double k_scale,
+                                     double v_scale) {
+  if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return -1;
+  if (!dtype_ok(q_dtype) || q_dtype == ORC_E4M3 || !dtype_ok(kv_dtype)) return -1;
+  if (query_start_loc[0] != 0 || query_start_loc[num_seqs] != total_q) return -1;
+  const int group = num_heads / num_kv_heads;
+  std::vector<double> qrow(head_dim);
+  std::vector<int> keys;
+  for (int s = 0; s < num_seqs; ++s) {
+    int q0 = query_start_loc[s], q_len = query_start_loc[s + 1] - q0;
+    int ctx = context_lens[s];
+    if (q_len < 0 || q_len > 64 || q_len > ctx || ctx > max_blocks_per_seq * block_size)
+      return -1;
+    const int32_t* table = block_tables + (size_t)s * max_blocks_per_seq;
+    const int base = ctx - q_len;
+    for (int i = 0; i < q_len; ++i) {
+      keys.clear();
+      for (int t = 0; t < base; ++t) keys.push_back(t);
+      for (int j = 0; j < q_len; ++j)
+        if ((tree_mask[q0 + i] >> j) & 1u) keys.push_back(base + j);
+      for (int h = 0; h < num_heads; ++h) {
+        size_t row = (size_t)(q0 + i) * num_heads + h;
+        for (int d = 0; d < head_dim; ++d)
+          qrow[d] = decode_elem((const uint8_t*)q, row * head_dim + d, q_dtype);
+        if (attend_keys(out + row * head_dim, qrow.data(), table, keys, k_cache, v_cache,
+                        h / group, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                        kv_dtype, k_scale, v_scale))
           return -2;
       }
     }

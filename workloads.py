@@ -252,6 +252,29 @@ def shared_prefix(name: str, seed: int, prompt_lens, tail_lens, H: int, Hkv: int
                      kv_dtype if kv_dtype != E4M3 else q_dtype, seed, groups=groups)
 
 
+# ---- draft trees (speculative verification) ------------------------------------
+def random_tree(r, n: int) -> np.ndarray:
+    """Parents of an n-node draft tree in topological order: node 0 is the
+    root (parent -1), every other node's parent has a smaller index."""
+    parents = np.full(n, -1, np.int64)
+    for i in range(1, n):
+        parents[i] = r.integers(0, i)
+    return parents
+
+
+def tree_mask(parents) -> np.ndarray:
+    """Per node, a 64-bit mask of the chunk keys it may see: itself and its
+    ancestors (bit j = node j).  A chain (parent i - 1) gives bits 0..i."""
+    n = len(parents)
+    assert n <= 64
+    m = np.zeros(n, np.uint64)
+    for i in range(n):
+        m[i] = np.uint64(1) << np.uint64(i)
+        if parents[i] >= 0:
+            m[i] |= m[parents[i]]
+    return m
+
+
 # ---- the named workloads ------------------------------------------------------
 def tiny(seed: int = 0) -> Workload:
     """4 sequences, 4 q heads = 4 kv heads, head_dim 64, fp16, 64-block pool,
