@@ -211,6 +211,38 @@ int pkv_paged_attention_prefill_chunk(void* out, const void* q, const void* k_ca
                                       uint32_t* device_errors, void* stream);
 
 /*
+ * Draft-tree verification: chunked-prefill attention in which each sequence's
+ * chunk is a tree of at most 64 draft tokens (speculative decoding, verified
+ * in one pass), and each draft token sees the context before the chunk plus
+ * only its own ancestors and itself.
+ * Sources: openeuler.csdn.net PagedAttention notes, "MEDUSA推理框架",
+ * "Tree Attention：" (candidate tokens of several heads form a tree verified
+ * under one attention mask) and "EAGLE2推理", "重排阶段" (the mask lets each
+ * token see only its ancestors).
+ *
+ *   tree_mask  [total_q] uint64: for the query at row query_start_loc[s] + i,
+ *              bit j set = the chunk's token j (position context_lens[s] -
+ *              q_len_s + j) is visible to it.  Bits 0..i for every i give
+ *              ordinary causal chunk attention.  Bits past the chunk are ignored.
+ *   max_q_len  at most 64 (PKV_ERR_INVALID_ARG otherwise); a longer chunk
+ *              found on the device is cut to 64 queries and flagged
+ *              PKV_DEVERR_CONTEXT.
+ *   Supported: 16-bit caches (kv_dtype == q_dtype), head_dim 128, query heads
+ *   per KV head dividing 128, at most 1024 sequences; otherwise
+ *   PKV_ERR_UNSUPPORTED.  No workspace.  Other arguments as for
+ *   pkv_paged_attention_prefill_chunk.
+ */
+int pkv_paged_attention_prefill_tree(void* out, const void* q, const void* k_cache,
+                                     const void* v_cache, const int32_t* block_tables,
+                                     const int32_t* context_lens, const int32_t* query_start_loc,
+                                     const uint64_t* tree_mask, int num_seqs, int total_q,
+                                     int max_q_len, int num_heads, int num_kv_heads, int head_dim,
+                                     int block_size, int max_blocks_per_seq, int num_blocks,
+                                     int max_context_len, float scale, pkv_dtype q_dtype,
+                                     pkv_dtype kv_dtype, float k_scale, float v_scale,
+                                     uint32_t* device_errors, void* stream);
+
+/*
  * Bytes of device workspace pkv_paged_attention_decode_cascade needs.
  */
 size_t pkv_cascade_workspace_size(int num_seqs, int num_heads, int head_dim,

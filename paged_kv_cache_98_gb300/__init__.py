@@ -82,6 +82,9 @@ def load():
             lib.pkv_paged_attention_decode_noalloc.restype = _I
             lib.pkv_paged_attention_decode_noalloc.argtypes = (
                 [_P] * 6 + [_I] * 8 + [_F, _I, _I, _F, _F, _I, _P, _P])
+            lib.pkv_paged_attention_prefill_tree.restype = _I
+            lib.pkv_paged_attention_prefill_tree.argtypes = (
+                [_P] * 8 + [_I] * 10 + [_F, _I, _I, _F, _F, _P, _P])
             lib.pkv_cascade_workspace_size.restype = _SZ
             lib.pkv_cascade_workspace_size.argtypes = [_I] * 5
             lib.pkv_paged_attention_decode_cascade.restype = _I
@@ -194,6 +197,31 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
         _dtype_code(k_cache), k_scale, v_scale, partition_size, _ptr(ws), wsb,
         _ptr(device_errors), _stream(stream))
     _check("pkv_paged_attention_decode", rc)
+    return out
+
+
+def paged_attention_prefill_tree(out, q, k_cache, v_cache, block_tables, context_lens,
+                                 query_start_loc, tree_mask, scale: float,
+                                 max_q_len: int | None = None, max_context_len: int | None = None,
+                                 device_errors=None, stream=None):
+    """Chunk attention under draft-tree masks (see
+    pkv_paged_attention_prefill_tree in include/pagedkv.h): tree_mask is a
+    [total_q] int64/uint64 tensor, bit j = the chunk's token j is visible."""
+    _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc, tree_mask,
+               device_errors)
+    TQ, H, D = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    S = query_start_loc.numel() - 1
+    if max_q_len is None:
+        max_q_len = int((query_start_loc[1:] - query_start_loc[:-1]).max().item()) if S else 0
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if S else 0
+    rc = load().pkv_paged_attention_prefill_tree(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        _ptr(query_start_loc), _ptr(tree_mask), S, TQ, max_q_len, H, hkv, D, bs,
+        block_tables.shape[1], nb, max_context_len, scale, _dtype_code(q), _dtype_code(k_cache),
+        1.0, 1.0, _ptr(device_errors), _stream(stream))
+    _check("pkv_paged_attention_prefill_tree", rc)
     return out
 
 

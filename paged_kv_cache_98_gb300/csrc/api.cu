@@ -259,6 +259,50 @@ int pkv_paged_attention_prefill_chunk(void* out, const void* q, const void* k_ca
                        workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
+int pkv_paged_attention_prefill_tree(void* out, const void* q, const void* k_cache,
+                                     const void* v_cache, const int32_t* block_tables,
+                                     const int32_t* context_lens, const int32_t* query_start_loc,
+                                     const uint64_t* tree_mask, int num_seqs, int total_q,
+                                     int max_q_len, int num_heads, int num_kv_heads, int head_dim,
+                                     int block_size, int max_blocks_per_seq, int num_blocks,
+                                     int max_context_len, float scale, pkv_dtype q_dtype,
+                                     pkv_dtype kv_dtype, float k_scale, float v_scale,
+                                     uint32_t* device_errors, void* stream) {
+  int rc = check_attention_args(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                num_heads, num_kv_heads, head_dim, block_size,
+                                max_blocks_per_seq, num_blocks, max_context_len, scale, q_dtype,
+                                kv_dtype, k_scale, v_scale);
+  if (rc != PKV_OK) return rc;
+  if (!query_start_loc || !tree_mask || total_q < 0 || max_q_len < 0 || max_q_len > 64)
+    return PKV_ERR_INVALID_ARG;
+  if (num_seqs == 0 || total_q == 0) return PKV_OK;
+  pkv::AttnParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.query_start_loc = query_start_loc;
+  p.tree_mask = tree_mask;
+  p.num_seqs = num_seqs;
+  p.num_rows = total_q;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_heads / num_kv_heads;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.partition = kDefaultPartition;
+  p.max_parts = parts_for(max_context_len, kDefaultPartition);
+  if (p.max_parts > 16384) return PKV_ERR_UNSUPPORTED;
+  p.errors = device_errors;
+  // the tensor-core prefill kernel carries the mask; other shapes are unsupported
+  if (!pkv::tc_prefill_supported(p, q_dtype, kv_dtype, head_dim)) return PKV_ERR_UNSUPPORTED;
+  p.q_scale = scale * pkv::kLog2e;
+  p.v_scale = 1.0f;
+  return pkv::launch_prefill_tc(p, q_dtype, total_q, static_cast<cudaStream_t>(stream));
+}
+
 size_t pkv_cascade_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len,
                                   int max_prefix_len) {
   if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||

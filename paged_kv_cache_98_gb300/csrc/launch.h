@@ -44,6 +44,9 @@ struct AttnParams {
   int prefix_chunk;               // keys per partial of the shared-prefix pass (multiple of 512)
   int non_causal;                 // prefill: every query sees all keys of its context
   int partial_out;                // prefill: write (o, lse) partials, one slot per key chunk
+  // Draft-tree verification (prefill): per query row, bit j = the chunk's key
+  // j is visible (its ancestors and itself); null = causal.
+  const uint64_t* tree_mask;
 };
 
 int launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,

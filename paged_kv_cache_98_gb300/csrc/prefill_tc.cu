@@ -36,6 +36,14 @@
 // the alternating MMAs take them in, so a V tile waiting for its softmax does
 // not hold back the next score tile's K.
 //
+// Draft-tree mode (speculative verification): a chunk of at most 64 draft
+// tokens whose queries each see the prior context and, of the chunk's own
+// keys, only those in their row of a 64-bit ancestor mask.  A draft token may
+// see only a handful of keys, where rounding its softmax weights to 16 bits no
+// longer averages out; in this mode each weight is also kept as a second
+// 16-bit term (the rounding remainder, in the other 64 columns of S) and P V
+// is accumulated from both, for about 16 significant bits.
+//
 // Warps: 0-3 softmax + epilogue of tile a, 4-7 of tile b, 8 TMEM owner + MMA
 // issuer, 9-11 TMA producers.  A K/V tile is 16 boxes of 16 rows x 128 B (one
 // per block and half); the boxes of each tile are spread over the three
@@ -202,6 +210,16 @@ __device__ __forceinline__ bool all_group(bool ok, int x) {
 }
 
 template <class QT>
+__device__ __forceinline__ float2 unpack2(uint32_t u) {
+  if constexpr (std::is_same<QT, BF16>::value) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+  } else {
+    __half2 h = *reinterpret_cast<__half2*>(&u);
+    return __half22float2(h);
+  }
+}
+
+template <class QT>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
   if constexpr (std::is_same<QT, BF16>::value) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -224,7 +242,8 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
-template <class QT>
+// kTree: draft-tree mode (per-row ancestor masks over the chunk's keys)
+template <class QT, bool kTree>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
@@ -281,10 +300,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         int qlen = __ldg(p.query_start_loc + sq + 1) - q0;
         int ctx = __ldg(p.context_lens + (p.seq_rows ? __ldg(p.seq_rows + sq) : sq));
         if (ctx < 0 || ctx > cap || qlen < 0 || (!p.non_causal && qlen > ctx) || q0 < 0 ||
-            q0 + qlen > p.num_rows) {
+            q0 + qlen > p.num_rows || (kTree && qlen > 64)) {
           flag_error(p.errors, PKV_DEVERR_CONTEXT);
           ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
           qlen = qlen < 0 ? 0 : (!p.non_causal && qlen > ctx ? ctx : qlen);
+          if (kTree && qlen > 64) qlen = 64;  // the mask covers 64 chunk keys
           if (q0 < 0 || q0 + qlen > p.num_rows) qlen = 0;
         }
         sm.seq_qlen[sq] = qlen;
@@ -514,6 +534,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t b = kk == ts ? dtail : dv + (uint64_t)((kk * (kBlockSize * 128)) >> 4);
           mma_f16_tmem_a(d, a + kk * 8, b, kIdescO, (t != x.first[qt]) || kk != 0);
         }
+        if (kTree) {  // the weights' rounding remainders
+#pragma unroll
+          for (int kk = 0; kk < kTileKeys / 16; ++kk) {
+            const uint64_t b =
+                kk == ts ? dtail : dv + (uint64_t)((kk * (kBlockSize * 128)) >> 4);
+            mma_f16_tmem_a(d, a + 64 + kk * 8, b, kIdescO, 1u);
+          }
+        }
         if (t == x.last[qt]) tc::mma_commit(&sm.o_done[qt]);
         return true;
       };
@@ -637,6 +665,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const int qpos = x.pos0[qt] + (p.non_causal ? 0 : tok);
+      // draft-tree mode: the row's visible chunk keys, from the chunk's first position
+      const int cbase = x.pos0[qt] - x.t0[qt];
+      const uint64_t tmask =
+          kTree && valid ? __ldg(p.tree_mask + x.q0 + x.t0[qt] + tok) : 0ull;
       float m_run = -INFINITY;
       float l8[8];  // partial row sums (independent chains)
 #pragma unroll
@@ -657,7 +689,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         float mx[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-        if (kbase + kTileKeys - 1 > x.pos0[qt]) {
+        if (kTree && kbase + kTileKeys - 1 >= cbase) {
+          // Chunk keys in this tile are visible when the row's mask has their
+          // bit; keys before the chunk always are.  Visibility of the tile's
+          // 128 keys as four 32-bit words: key 32 w + i is bit i of vw[w].
+          const int nrel = x.ctx - cbase;  // keys in the chunk (<= 64)
+          uint32_t vw[4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const int r0 = kbase + 32 * w - cbase;  // chunk index of the word's first key
+            const uint64_t bits = r0 >= 0 ? (r0 < 64 ? tmask >> r0 : 0ull)
+                                          : (-r0 < 64 ? tmask << -r0 : 0ull);
+            const int lim = nrel - r0;  // keys i < lim are before the chunk's end
+            const uint32_t keep = lim <= 0 ? 0u : (lim >= 32 ? ~0u : (1u << lim) - 1u);
+            const uint32_t prior = r0 >= 0 ? 0u : (-r0 >= 32 ? ~0u : (1u << -r0) - 1u);
+            vw[w] = prior | ((uint32_t)bits & keep);
+          }
+#pragma unroll
+          for (int c = 0; c < kTileKeys; ++c) {
+            sv[c] = (vw[c >> 5] >> (c & 31)) & 1u ? sv[c] : -INFINITY;
+            mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
+          }
+        } else if (kbase + kTileKeys - 1 > x.pos0[qt]) {
           // the causal boundary crosses this tile: hidden keys become -inf
 #pragma unroll
           for (int c = 0; c < kTileKeys; ++c) {
@@ -681,20 +734,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) l8[i] *= alpha;
         }
-        // P over the first 64 columns of S: keys 2c and 2c+1 in column c
+        // P over the first 64 columns of S: keys 2c and 2c+1 in column c; in
+        // draft-tree mode the rounding remainders over the other 64
+        if (!kTree) {
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          float pk[16];
+          for (int h = 0; h < 4; ++h) {
+            float pk[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int k0 = h * 32 + 2 * c;
-            const float e0 = fast_exp2(fmaf(sv[k0], qa, -m_run));
-            const float e1 = fast_exp2(fmaf(sv[k0 + 1], qa, -m_run));
-            l8[(2 * c) & 7] += e0;
-            l8[(2 * c + 1) & 7] += e1;
-            pk[c] = __uint_as_float(pack2<QT>(e0, e1));
+            for (int c = 0; c < 16; ++c) {
+              const int k0 = h * 32 + 2 * c;
+              const float e0 = fast_exp2(fmaf(sv[k0], qa, -m_run));
+              const float e1 = fast_exp2(fmaf(sv[k0 + 1], qa, -m_run));
+              l8[(2 * c) & 7] += e0;
+              l8[(2 * c + 1) & 7] += e1;
+              pk[c] = __uint_as_float(pack2<QT>(e0, e1));
+            }
+            tc::tmem_st16(s_col + 16 * h, pk);
           }
-          tc::tmem_st16(s_col + 16 * h, pk);
+        } else {
+#pragma unroll
+          for (int h = 0; h < 8; ++h) {  // 16 keys at a time: weights, then remainders
+            float pk[8], pl[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const int k0 = h * 16 + 2 * c;
+              const float e0 = fast_exp2(fmaf(sv[k0], qa, -m_run));
+              const float e1 = fast_exp2(fmaf(sv[k0 + 1], qa, -m_run));
+              l8[(2 * c) & 7] += e0;
+              l8[(2 * c + 1) & 7] += e1;
+              const uint32_t hi = pack2<QT>(e0, e1);
+              const float2 r = unpack2<QT>(hi);
+              pk[c] = __uint_as_float(hi);
+              pl[c] = __uint_as_float(pack2<QT>(e0 - r.x, e1 - r.y));
+            }
+            tc::tmem_st8(s_col + 8 * h, pk);
+            tc::tmem_st8(s_col + 64 + 8 * h, pl);
+          }
         }
         // the product of tile t adds onto O: rescale it first when a row's max moved
         if (t > x.first[qt] && __any_sync(kFull, need)) {
@@ -784,13 +859,14 @@ int launch_typed(const AttnParams& p, int total_q, cudaStream_t stream) {
                 "swizzled buffers must start on 1024-byte boundaries");
   static_assert(offsetof(Smem, q) == offsetof(Smem, ring) + kStages * kTileBytes,
                 "q[0] is the ring's fifth stage in shared-prefix mode");
-  auto kern = prefill_tc_kernel<QT>;
-  static bool configured = false;
-  if (!configured) {
+  const bool tree = p.tree_mask != nullptr;
+  auto kern = tree ? prefill_tc_kernel<QT, true> : prefill_tc_kernel<QT, false>;
+  static bool configured[2] = {false, false};
+  if (!configured[tree]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return PKV_ERR_CUDA;
-    configured = true;
+    configured[tree] = true;
   }
   // an upper bound of the items: every sequence's tile pairs, times the KV heads
   const long long tiles = ((long long)total_q * p.group + (long long)p.num_seqs * (kRowsM - 1)) /

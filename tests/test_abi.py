@@ -147,3 +147,14 @@ def test_cascade_workspace_size(lib):
     assert pkv.cascade_workspace_size(64, 32, 128, 4096, 5000) == want
     # always a workspace, even for one partition and no prefix
     assert pkv.cascade_workspace_size(1, 8, 128, 16, 0) > 0
+
+
+def test_tree_argument_validation(lib):
+    f = lib.pkv_paged_attention_prefill_tree
+    args = [256, 256, 512, 512, 1024, 2048, 4096, 8192, 1, 10, 10, 8, 2, 128, 16, 4, 8, 64, 0.1,
+            1, 1, 1.0, 1.0, None, None]
+    assert f(*args[:7], None, *args[8:]) == -1  # no mask
+    long = list(args)
+    long[10] = 65  # max_q_len above 64
+    assert f(*long) == -1
+    assert f(*args[:8], 0, *args[9:]) == 0  # no sequences

@@ -1,0 +1,100 @@
+"""Draft-tree chunk attention (pkv_paged_attention_prefill_tree) vs the CPU
+oracle's tree-masked attention: |gpu - ref| <= 2e-3 + 1e-2 |ref|."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_98_gb300 as pkv
+import workloads
+from _gpu import bits_to_dev, cache_tensors, check_close, fill_device_cache, tol
+from _util import host_cache
+
+pytestmark = pytest.mark.gpu
+F16, BF16 = workloads.F16, workloads.BF16
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    from paged_kv_cache_98_gb300 import _build
+    _build.build()
+    pkv.load()
+    torch.cuda.init()
+
+
+def all_inputs(w, q_all):
+    """Every sequence's queries (chunks of any length, single tokens included)."""
+    dev = q_all.device
+    bt = torch.from_numpy(np.ascontiguousarray(w.block_tables)).to(dev)
+    cl = torch.from_numpy(np.ascontiguousarray(w.context_lens)).to(dev)
+    qsl = torch.from_numpy(workloads.query_start_loc(w.q_lens)).to(dev)
+    return q_all.contiguous(), bt, cl, qsl
+
+
+def run_tree(w, masks, sentinel=0xFF):
+    k, v, q = workloads.values_cpu(w)
+    kc_h, vc_h = host_cache(w, k, v)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kc, vc = cache_tensors(w, sentinel=sentinel)
+    fill_device_cache(w, bits_to_dev(k, w.src_dtype), bits_to_dev(v, w.src_dtype), kc, vc,
+                      errors=err)
+    qq, bt, cl, qsl_d = all_inputs(w, bits_to_dev(q, w.q_dtype))
+    out = torch.empty_like(qq)
+    tm = torch.from_numpy(masks.view(np.int64)).cuda()
+    pkv.paged_attention_prefill_tree(out, qq, kc, vc, bt, cl, qsl_d, tm, w.scale,
+                                     device_errors=err)
+    assert pkv.check_errors(err) == 0
+    ref = oracle.paged_attention_prefill_tree(np.ascontiguousarray(q), kc_h, vc_h, w.block_tables,
+                                              w.context_lens, workloads.query_start_loc(w.q_lens),
+                                              masks, w.num_kv_heads, w.head_dim, 16, w.num_blocks,
+                                              w.scale, w.q_dtype, w.kv_dtype)
+    check_close(out.float().cpu().numpy(), ref, tol(w), f"{w.name} tree")
+    return out, ref
+
+
+@pytest.mark.parametrize("g,dt", [(4, BF16), (8, F16), (1, BF16)])
+def test_random_draft_trees(g, dt):
+    r = np.random.default_rng(7 + g)
+    qlens = [64, 7, 33, 1, 20]
+    prior = [300, 0, 16, 1000, 2049]
+    w = workloads.independent("tree", 60 + g, [a + b for a, b in zip(qlens, prior)], 2 * g, 2,
+                              128, dt, dt, q_lens=qlens)
+    masks = []
+    for n in qlens:
+        parents = workloads.random_tree(r, n)
+        if n == 33:
+            parents[1:] = 0  # a star
+        masks.append(workloads.tree_mask(parents))
+    run_tree(w, np.concatenate(masks))
+
+
+def test_chain_equals_causal_chunk():
+    """A chain-shaped tree is the causal chunk.  Tree mode splits each weight
+    into a 16-bit value and its rounding remainder, so on average it is as close
+    to the exact result as the causal kernel, and both meet the tolerance."""
+    qlens = [64, 30]
+    w = workloads.independent("tree-chain", 70, [600, 95], 16, 2, 128, BF16, BF16, q_lens=qlens)
+    masks = np.concatenate([workloads.tree_mask(np.arange(n) - 1) for n in qlens])
+    out_t, ref = run_tree(w, masks)
+    k, v, q = workloads.values_cpu(w)
+    kc, vc = cache_tensors(w)
+    fill_device_cache(w, bits_to_dev(k, BF16), bits_to_dev(v, BF16), kc, vc)
+    qq, bt, cl, qsl_d = all_inputs(w, bits_to_dev(q, BF16))
+    out_c = torch.empty_like(qq)
+    pkv.paged_attention_prefill_chunk(out_c, qq, kc, vc, bt, cl, qsl_d, w.scale,
+                                      max_q_len=64, max_context_len=600)
+    check_close(out_c.float().cpu().numpy(), ref, tol(w), "causal chunk")
+    err_t = np.abs(out_t.float().cpu().numpy() - ref).mean()
+    err_c = np.abs(out_c.float().cpu().numpy() - ref).mean()
+    assert err_t <= 1.02 * err_c
+
+
+def test_unsupported_and_invalid():
+    w = workloads.independent("tree-x", 71, [80], 8, 2, 128, BF16, BF16, q_lens=[65])
+    k, v, q = workloads.values_cpu(w)
+    kc, vc = cache_tensors(w)
+    qq, bt, cl, qsl_d = all_inputs(w, bits_to_dev(q, BF16))
+    out = torch.empty_like(qq)
+    tm = torch.zeros(65, dtype=torch.int64, device="cuda")
+    with pytest.raises(pkv.PagedKVError):  # a chunk longer than 64
+        pkv.paged_attention_prefill_tree(out, qq, kc, vc, bt, cl, qsl_d, tm, w.scale)
