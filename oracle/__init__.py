@@ -97,6 +97,32 @@ def _declare(L):
     L.orc_seq_table.argtypes = [_P, _P, _I]
     L.orc_seq_slot.restype = _I64
     L.orc_seq_slot.argtypes = [_P, _I]
+    L.orc_cpool_create.restype = _P
+    L.orc_cpool_create.argtypes = [_I, _I]
+    L.orc_cpool_destroy.restype = None
+    L.orc_cpool_destroy.argtypes = [_P]
+    for name in ("orc_cpool_num_free", "orc_cpool_num_cached"):
+        getattr(L, name).restype = _I
+        getattr(L, name).argtypes = [_P]
+    for name in ("orc_cpool_ref_cnt", "orc_cpool_is_cached"):
+        getattr(L, name).restype = _I
+        getattr(L, name).argtypes = [_P, _I]
+    L.orc_cpool_queue.restype = _I
+    L.orc_cpool_queue.argtypes = [_P, _P, _I]
+    L.orc_creq_create.restype = _P
+    L.orc_creq_create.argtypes = [_P]
+    L.orc_creq_match.restype = _I
+    L.orc_creq_match.argtypes = [_P, _P, _I]
+    L.orc_creq_append.restype = _I
+    L.orc_creq_append.argtypes = [_P, _P, _I, _P, _P]
+    L.orc_creq_fork.restype = _P
+    L.orc_creq_fork.argtypes = [_P]
+    L.orc_creq_free.restype = None
+    L.orc_creq_free.argtypes = [_P]
+    L.orc_creq_num_tokens.restype = _I
+    L.orc_creq_num_tokens.argtypes = [_P]
+    L.orc_creq_table.restype = _I
+    L.orc_creq_table.argtypes = [_P, _P, _I]
     L.orc_reshape_and_cache.restype = _I
     L.orc_reshape_and_cache.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F]
     L.orc_paged_attention_decode.restype = _I
@@ -230,6 +256,91 @@ class Seq:
     def free(self):
         if self.h:
             lib().orc_seq_destroy(self.h)
+            self.h = None
+
+
+# ---- prefix-caching pool ----------------------------------------------------
+class CachePool:
+    """Block pool with prefix caching: registered full blocks stay matchable at
+    reference count 0 until the LRU free queue hands them out again."""
+
+    def __init__(self, num_blocks: int, block_size: int = 16):
+        self.h = lib().orc_cpool_create(num_blocks, block_size)
+        if not self.h:
+            raise OracleError("bad pool arguments")
+        self.num_blocks, self.block_size = num_blocks, block_size
+
+    def num_free(self) -> int:
+        return lib().orc_cpool_num_free(self.h)
+
+    def num_cached(self) -> int:
+        return lib().orc_cpool_num_cached(self.h)
+
+    def ref_cnt(self, i: int) -> int:
+        return lib().orc_cpool_ref_cnt(self.h, i)
+
+    def is_cached(self, i: int) -> bool:
+        return lib().orc_cpool_is_cached(self.h, i) == 1
+
+    def queue(self) -> np.ndarray:
+        out = np.empty(max(self.num_blocks, 1), dtype=np.int32)
+        n = lib().orc_cpool_queue(self.h, _ptr(out), self.num_blocks)
+        return out[:n]
+
+    def request(self) -> "CacheReq":
+        return CacheReq(self, lib().orc_creq_create(self.h))
+
+    def close(self):
+        if self.h:
+            lib().orc_cpool_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class CacheReq:
+    """One request's tokens and block table in a CachePool."""
+
+    def __init__(self, pool: CachePool, handle):
+        self.pool, self.h = pool, handle
+
+    def match(self, tokens) -> int:
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        m = lib().orc_creq_match(self.h, _ptr(t), len(t))
+        if m < 0:
+            raise OracleError("match on a request that already holds tokens")
+        return m
+
+    def append(self, ids):
+        """Returns (slots, cow) where cow is (source, copy) or None; raises
+        OracleError (nothing changed) when the pool is out of blocks."""
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        slots = np.empty(max(len(ids), 1), dtype=np.int64)
+        cow = np.empty(2, dtype=np.int32)
+        if lib().orc_creq_append(self.h, _ptr(ids), len(ids), _ptr(slots), _ptr(cow)) != 0:
+            raise OracleError("block pool exhausted")
+        return slots[:len(ids)], (None if cow[0] < 0 else (int(cow[0]), int(cow[1])))
+
+    def fork(self) -> "CacheReq":
+        return CacheReq(self.pool, lib().orc_creq_fork(self.h))
+
+    @property
+    def num_tokens(self) -> int:
+        return lib().orc_creq_num_tokens(self.h)
+
+    def table(self) -> np.ndarray:
+        n = lib().orc_creq_table(self.h, None, 0)
+        out = np.empty(max(n, 1), dtype=np.int32)
+        lib().orc_creq_table(self.h, _ptr(out), n)
+        return out[:n]
+
+    def free(self):
+        if self.h:
+            lib().orc_creq_free(self.h)
             self.h = None
 
 

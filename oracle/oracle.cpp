@@ -16,7 +16,8 @@
 //        "Attention 计算时的 Block 映射（CUDA Kernel 伪代码）".
 //  [P1]  "第34讲 … vLLM 生产级系统架构全景剖析与四重加速引擎", §1.2
 //        (KVCacheManager.allocate_slots / free in reverse order, BlockPool,
-//        ref_cnt), §4.4 (FP8 E4M3 KV cache).
+//        ref_cnt, FreeKVCacheBlockQueue), §2.2 (longest-prefix match, ref_cnt),
+//        §2.3 (cached-free blocks, LRU eviction), §4.4 (FP8 E4M3 KV cache).
 //  [P3]  "第32讲 … Prefill vs Decode …", §3.1 (softmax(QK^T/sqrt(d_k))V and
 //        the decode step), §3.2 (per-token KV bytes), §3.4 (GQA grouping),
 //        §5.4 (chunked prefill).
@@ -39,6 +40,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <vector>
 
 namespace {
@@ -659,6 +661,209 @@ int orc_paged_attention_prefill_tree(double* out, const void* q, const uint8_t* 
     }
   }
   return 0;
+}
+
+}  // extern "C"
+
+// ===========================================================================
+// Prefix-caching block pool ([P1] §1.2 BlockPool, FreeKVCacheBlockQueue,
+// KVCacheManager.allocate_slots / free; §2.2 longest-prefix match with ref_cnt;
+// §2.3 cached-free blocks and LRU eviction).
+//
+// Written for plainness, not speed: the free queue is a vector searched
+// linearly, and a cached block is keyed by its whole token prefix (every token
+// from the sequence's start through the block's last), so equal keys mean
+// equal contents by definition.
+//
+// Readings where the pages are silent:
+//  * only full blocks are cached; a block is registered when its last slot is
+//    filled;
+//  * when a prefix is already registered to another block, the new block
+//    stays unregistered (the first copy keeps serving hits);
+//  * a match stops before the block holding the prompt's last token, so at
+//    least one token is always left to compute;
+//  * every block whose count drops to 0 goes to the queue's tail, registered
+//    or not; allocation takes the head and drops the head's registration
+//    (eviction).  A fresh pool's queue holds blocks 0, 1, 2, ... in order.
+namespace {
+
+struct CachePool {
+  int num_blocks = 0, block_size = 0;
+  std::vector<int> queue;                    // free blocks; front = next out
+  std::vector<int> ref_cnt;
+  std::vector<std::vector<int32_t>> key;     // registered prefix (empty: none)
+  std::map<std::vector<int32_t>, int> cached;  // prefix -> block
+};
+
+struct CacheReq {
+  CachePool* pool = nullptr;
+  std::vector<int32_t> tokens;  // the request's tokens so far
+  std::vector<int> table;       // logical block -> physical block
+};
+
+// A block leaves the free queue (wherever it is) and gains a reference.
+void cp_take(CachePool* p, int id) {
+  if (p->ref_cnt[id] == 0) {
+    for (size_t i = 0; i < p->queue.size(); ++i) {
+      if (p->queue[i] == id) {
+        p->queue.erase(p->queue.begin() + i);
+        break;
+      }
+    }
+  }
+  ++p->ref_cnt[id];
+}
+
+// The head of the queue, its registration dropped; -1 when the queue is empty.
+int cp_alloc(CachePool* p) {
+  if (p->queue.empty()) return -1;
+  int id = p->queue.front();
+  p->queue.erase(p->queue.begin());
+  if (!p->key[id].empty()) {
+    p->cached.erase(p->key[id]);
+    p->key[id].clear();
+  }
+  p->ref_cnt[id] = 1;
+  return id;
+}
+
+void cp_release(CachePool* p, int id) {
+  if (--p->ref_cnt[id] == 0) p->queue.push_back(id);
+}
+
+}  // namespace
+
+extern "C" {
+
+void* orc_cpool_create(int num_blocks, int block_size) {
+  if (num_blocks < 0 || block_size <= 0) return nullptr;
+  CachePool* p = new CachePool;
+  p->num_blocks = num_blocks;
+  p->block_size = block_size;
+  p->ref_cnt.assign(num_blocks, 0);
+  p->key.assign(num_blocks, {});
+  for (int i = 0; i < num_blocks; ++i) p->queue.push_back(i);
+  return p;
+}
+
+void orc_cpool_destroy(void* pool) { delete (CachePool*)pool; }
+int orc_cpool_num_free(void* pool) { return (int)((CachePool*)pool)->queue.size(); }
+int orc_cpool_num_cached(void* pool) { return (int)((CachePool*)pool)->cached.size(); }
+
+int orc_cpool_ref_cnt(void* pool, int id) {
+  CachePool* p = (CachePool*)pool;
+  return id < 0 || id >= p->num_blocks ? -1 : p->ref_cnt[id];
+}
+
+// 1 when the block holds a registered prefix, 0 when not, -1 for a bad id.
+int orc_cpool_is_cached(void* pool, int id) {
+  CachePool* p = (CachePool*)pool;
+  return id < 0 || id >= p->num_blocks ? -1 : (p->key[id].empty() ? 0 : 1);
+}
+
+// Copies up to max entries of the free queue, head first; returns its length.
+int orc_cpool_queue(void* pool, int32_t* out, int max) {
+  CachePool* p = (CachePool*)pool;
+  int n = (int)p->queue.size();
+  for (int i = 0; i < n && i < max; ++i) out[i] = p->queue[i];
+  return n;
+}
+
+void* orc_creq_create(void* pool) {
+  if (!pool) return nullptr;
+  CacheReq* r = new CacheReq;
+  r->pool = (CachePool*)pool;
+  return r;
+}
+
+// Longest cached prefix of tokens[0..n) in whole blocks, for a request that
+// holds no tokens yet: each hit block gains a reference (leaving the free
+// queue if it was there) and joins the table.  Returns the number of tokens
+// matched (a multiple of block_size, at most n - 1), or -1 if the request is
+// not empty.
+int orc_creq_match(void* req, const int32_t* tokens, int n) {
+  CacheReq* r = (CacheReq*)req;
+  CachePool* p = r->pool;
+  if (!r->tokens.empty() || !r->table.empty()) return -1;
+  int matched = 0;
+  for (int end = p->block_size; end <= n - 1; end += p->block_size) {
+    std::vector<int32_t> prefix(tokens, tokens + end);
+    auto it = p->cached.find(prefix);
+    if (it == p->cached.end()) break;
+    cp_take(p, it->second);
+    r->table.push_back(it->second);
+    matched = end;
+  }
+  r->tokens.assign(tokens, tokens + matched);
+  return matched;
+}
+
+// Appends n tokens with the given ids ([P1] §1.2 allocate_slots): the last
+// block is filled first, then new blocks are taken from the queue's head.  If
+// the last block is partial and shared with a forked request, it is copied
+// on write first: cow_out (may be NULL) receives {source, copy}, or {-1, -1}
+// when no copy was needed.  slots_out (may be NULL) receives each token's
+// slot.  Blocks that become full are registered under their prefix.
+// All or nothing: returns -1, changing nothing, when the queue holds fewer
+// blocks than the append needs; 0 otherwise.
+int orc_creq_append(void* req, const int32_t* ids, int n, int64_t* slots_out, int32_t* cow_out) {
+  CacheReq* r = (CacheReq*)req;
+  CachePool* p = r->pool;
+  const int bs = p->block_size;
+  const int t0 = (int)r->tokens.size();
+  if (cow_out) cow_out[0] = cow_out[1] = -1;
+  if (n <= 0) return n == 0 ? 0 : -1;
+  const bool cow = t0 % bs != 0 && p->ref_cnt[r->table.back()] > 1;
+  int need = cow ? 1 : 0;
+  for (int pos = t0; pos < t0 + n; ++pos) need += pos % bs == 0 ? 1 : 0;
+  if (need > (int)p->queue.size()) return -1;
+  if (cow) {
+    const int old = r->table.back();
+    const int id = cp_alloc(p);
+    cp_release(p, old);
+    r->table.back() = id;
+    if (cow_out) {
+      cow_out[0] = old;
+      cow_out[1] = id;
+    }
+  }
+  for (int i = 0; i < n; ++i) {
+    const int pos = t0 + i;
+    if (pos % bs == 0) r->table.push_back(cp_alloc(p));
+    const int id = r->table[pos / bs];
+    if (slots_out) slots_out[i] = (int64_t)id * bs + pos % bs;
+    r->tokens.push_back(ids[i]);
+    if (pos % bs == bs - 1 && p->cached.find(r->tokens) == p->cached.end()) {
+      p->cached[r->tokens] = id;
+      p->key[id] = r->tokens;
+    }
+  }
+  return 0;
+}
+
+// A request sharing every block of req by reference ([P2] "机制 2：写时复制").
+void* orc_creq_fork(void* req) {
+  CacheReq* r = (CacheReq*)req;
+  CacheReq* c = new CacheReq(*r);
+  for (int id : c->table) ++c->pool->ref_cnt[id];
+  return c;
+}
+
+// Releases the request's blocks tail first ([P1] §1.2 free) and deletes it.
+void orc_creq_free(void* req) {
+  CacheReq* r = (CacheReq*)req;
+  if (!r) return;
+  for (int j = (int)r->table.size() - 1; j >= 0; --j) cp_release(r->pool, r->table[j]);
+  delete r;
+}
+
+int orc_creq_num_tokens(void* req) { return (int)((CacheReq*)req)->tokens.size(); }
+
+int orc_creq_table(void* req, int32_t* out, int max) {
+  CacheReq* r = (CacheReq*)req;
+  int n = (int)r->table.size();
+  for (int j = 0; j < n && j < max; ++j) out[j] = r->table[j];
+  return n;
 }
 
 }  // extern "C"
