@@ -123,6 +123,8 @@ def _declare(L):
     L.orc_creq_num_tokens.argtypes = [_P]
     L.orc_creq_table.restype = _I
     L.orc_creq_table.argtypes = [_P, _P, _I]
+    L.orc_copy_blocks.restype = _I
+    L.orc_copy_blocks.argtypes = [_P, _P, _P, _I, _I, _I64]
     L.orc_reshape_and_cache.restype = _I
     L.orc_reshape_and_cache.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _F]
     L.orc_paged_attention_decode.restype = _I
@@ -342,6 +344,14 @@ class CacheReq:
         if self.h:
             lib().orc_creq_free(self.h)
             self.h = None
+
+
+def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, pairs, num_blocks: int):
+    """In-place copy of whole blocks (source, destination) in both uint8 caches."""
+    pr = np.ascontiguousarray(pairs, dtype=np.int32).reshape(-1, 2)
+    bb = k_cache.nbytes // num_blocks
+    _check(lib().orc_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(pr), len(pr), num_blocks, bb),
+           "orc_copy_blocks")
 
 
 # ---- cache write and attention ----------------------------------------------

@@ -841,6 +841,23 @@ int orc_creq_append(void* req, const int32_t* ids, int n, int64_t* slots_out, in
   return 0;
 }
 
+// The copy half of copy-on-write ([P2] "机制 2：写时复制": the writer gets a
+// private copy of the shared block before it writes): for each pair
+// (source, destination) in order, the destination block's bytes in each cache
+// become the source block's.  block_bytes is one block of one cache.
+// Returns 0, or -1 (nothing copied) when an id is outside the pool.
+int orc_copy_blocks(uint8_t* k_cache, uint8_t* v_cache, const int32_t* pairs, int num_pairs,
+                    int num_blocks, int64_t block_bytes) {
+  for (int i = 0; i < 2 * num_pairs; ++i)
+    if (pairs[i] < 0 || pairs[i] >= num_blocks) return -1;
+  for (int i = 0; i < num_pairs; ++i) {
+    const size_t src = (size_t)pairs[2 * i] * block_bytes, dst = (size_t)pairs[2 * i + 1] * block_bytes;
+    std::memmove(k_cache + dst, k_cache + src, (size_t)block_bytes);
+    std::memmove(v_cache + dst, v_cache + src, (size_t)block_bytes);
+  }
+  return 0;
+}
+
 // A request sharing every block of req by reference ([P2] "机制 2：写时复制").
 void* orc_creq_fork(void* req) {
   CacheReq* r = (CacheReq*)req;

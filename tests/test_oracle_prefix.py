@@ -257,3 +257,29 @@ def test_random_trace_content_and_queue_discipline(seed):
         q = set(p.queue().tolist())
         assert all((p.ref_cnt(b) == 0) == (b in q) for b in range(nb))
     assert hits > 0
+
+
+def test_copy_blocks_is_the_copy_of_copy_on_write():
+    """oracle.copy_blocks reproduces the bytes that the block-table sequence's
+    own copy-on-write (oracle.Seq.append with caches) writes, and touches no
+    other block."""
+    r = np.random.default_rng(3)
+    nb, bb = 12, 8 * 16 * 64 * 2  # 8 KV heads x 16 rows x 64 dims x 2 bytes
+    k0 = r.integers(0, 256, nb * bb, dtype=np.uint8)
+    v0 = r.integers(0, 256, nb * bb, dtype=np.uint8)
+    k1, v1 = k0.copy(), v0.copy()
+    pool = oracle.Pool(nb)
+    s = oracle.Seq(pool)
+    s.append(2 * BS + 3, caches=(k1, v1, bb))
+    c = s.fork()
+    before = s.table().copy()
+    c.append(1, caches=(k1, v1, bb))  # copies the shared partial block
+    src, dst = int(before[-1]), int(c.table()[-1])
+    assert src != dst
+    k2, v2 = k0.copy(), v0.copy()
+    oracle.copy_blocks(k2, v2, [[src, dst]], nb)
+    assert np.array_equal(k2, k1) and np.array_equal(v2, v1)
+    changed = np.flatnonzero((k2 != k0).reshape(nb, bb).any(axis=1))
+    assert set(changed.tolist()) <= {dst}
+    with pytest.raises(oracle.OracleError):
+        oracle.copy_blocks(k2, v2, [[0, nb]], nb)
