@@ -46,6 +46,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-also", action="store_true", help="skip the other workloads")
+    ap.add_argument("--decode-entry", default="plain", choices=["plain", "cascade"],
+                    help="decode through pkv_paged_attention_decode or, reading each shared "
+                         "prompt block once per group, pkv_paged_attention_decode_cascade")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--workload", default="llama2_7b",
@@ -61,6 +64,7 @@ TRAFFIC_PROFILES = {
     "llama2_7b": "decode_llama2_7b",
     "gqa70b_shared": "decode_gqa70b_shared_tc",
     "long_fp8": "decode_long_fp8_tc",
+    "gqa70b_shared+cascade": "decode_gqa70b_shared_cascade",
 }
 
 
@@ -167,7 +171,7 @@ class GpuStep:
     """Device-resident state of one workload and its step (cache write, decode
     attention, and prefill-chunk attention when the workload has chunks)."""
 
-    def __init__(self, w, dev):
+    def __init__(self, w, dev, cascade=False):
         import numpy as np
         import torch
 
@@ -220,6 +224,15 @@ class GpuStep:
             nb = pkv.prefill_workspace_size(self.q_pre.shape[0], H, D, self.max_ctx_pre,
                                             self.max_q_pre)
             self.ws_pre = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+        self.cascade = cascade
+        if cascade:
+            gs, pre = w.cascade_groups()
+            self.casc_mp = int(pre.max()) if len(pre) else 0
+            self.casc_ws = torch.empty(
+                max(256, pkv.cascade_workspace_size(S, H, D, self.max_ctx, self.casc_mp)),
+                dtype=torch.uint8, device=dev)
+            self.casc_gs = torch.from_numpy(gs).to(dev)
+            self.casc_pre = torch.from_numpy(pre).to(dev)
         del k, v, q
         torch.cuda.synchronize(dev)
         if pkv.check_errors(self.err) != 0:
@@ -260,7 +273,9 @@ class GpuStep:
 
     def launches_per_step(self) -> int:
         n = 1  # cache write
-        if len(self.dec):
+        if len(self.dec) and self.cascade:
+            n += 3  # shared-prefix pass, own-keys decode, merge
+        elif len(self.dec):
             n += 1 + (1 if self.parts > 1 else 0)
         if len(self.pre):
             n += 1 + (1 if -(-self.max_ctx_pre // 512) > 1 else 0)
@@ -271,7 +286,12 @@ class GpuStep:
                                    self.vs, device_errors=self.err)
 
     def decode(self):
-        if len(self.dec):
+        if len(self.dec) and self.cascade:
+            self.pkv.paged_attention_decode_cascade(
+                self.out, self.q_dec, self.kc, self.vc, self.bt, self.cl, self.casc_gs,
+                self.casc_pre, self.w.scale, max_context_len=self.max_ctx,
+                max_prefix_len=self.casc_mp, workspace=self.casc_ws, device_errors=self.err)
+        elif len(self.dec):
             self.pkv.paged_attention_decode(
                 self.out, self.q_dec, self.kc, self.vc, self.bt, self.cl, self.w.scale,
                 max_context_len=self.max_ctx, k_scale=self.ks, v_scale=self.vs, workspace=self.ws,
@@ -327,7 +347,10 @@ class GpuStep:
         inputs are copied in and its output read back inside the timed region."""
         import torch
         host = {}
-        for name in ("k_new", "v_new", "slots", "q_dec", "bt", "cl"):
+        names = ("k_new", "v_new", "slots", "q_dec", "bt", "cl")
+        if self.cascade:
+            names += ("casc_gs", "casc_pre")
+        for name in names:
             t = getattr(self, name)
             h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
             h.copy_(t)
@@ -467,7 +490,8 @@ def main():
             dist.barrier()
 
     w = workloads.NAMED[args.workload]()
-    st = GpuStep(w, dev)
+    cascade = args.decode_entry == "cascade"
+    st = GpuStep(w, dev, cascade=cascade)
     sampler = ClockSampler(local).start()
     time.sleep(0.3)
     res = st.timed(args.steps, args.warmup, barrier)
@@ -506,6 +530,7 @@ def main():
             "num_seqs": w.num_seqs, "context": int(w.context_lens.max()),
             "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
             "block_size": 16, "partition": 512, "pool_blocks": w.num_blocks,
+            "decode_entry": args.decode_entry,
             "kv_bytes_per_step": kv_bytes,
             "l2": f"inputs larger than L2: {kv_bytes / 1e9:.2f} GB of K/V read per step "
                   "vs 129 MB L2",
@@ -514,11 +539,14 @@ def main():
         "attended_tokens_per_s": round(world * tokens / (ms * 1e-3), 1),
         "hbm_frac": round(value / world / peak, 4),
         "roofline": {
-            "kernel": "paged decode attention (attention + log-sum-exp merge launches)",
+            "kernel": ("cascade decode (shared-prefix pass + own-keys decode + merge launches)"
+                       if cascade else
+                       "paged decode attention (attention + log-sum-exp merge launches)"),
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
             "peak_kind": f"{peak_kind} HBM copy bandwidth",
             "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "traffic": recorded_traffic(TRAFFIC_PROFILES.get(args.workload, "")),
+            "traffic": recorded_traffic(TRAFFIC_PROFILES.get(
+                args.workload + ("+cascade" if cascade else ""), "")),
             "algorithmic_bytes_per_launch": kv_bytes,
             "decode_ms": round(dec_ms, 5), "write_ms": round(res["write_ms"], 5),
         },

@@ -57,7 +57,8 @@ typedef enum {
   PKV_ERR_WORKSPACE = -3,   /* workspace missing or smaller than the size function says */
   PKV_ERR_CUDA = -4,        /* the CUDA runtime reported an error at launch */
   PKV_ERR_DEVICE = -5,      /* pkv_check_errors: a device-side check failed */
-  PKV_ERR_TIMEOUT = -6      /* pkv_check_errors: a device-side wait gave up */
+  PKV_ERR_TIMEOUT = -6,     /* pkv_check_errors: a device-side wait gave up */
+  PKV_ERR_NO_BLOCKS = -7    /* the block pool holds fewer free blocks than the call needs */
 } pkv_status;
 
 #define PKV_DEVERR_BLOCK_ID 0x1u    /* block table entry outside [0, num_blocks) */
@@ -288,6 +289,101 @@ int pkv_paged_attention_decode_cascade(void* out, const void* q, const void* k_c
                                        pkv_dtype q_dtype, pkv_dtype kv_dtype, float k_scale,
                                        float v_scale, void* workspace, size_t workspace_bytes,
                                        uint32_t* device_errors, void* stream);
+
+/*
+ * Whole-block copies in both caches: the device half of copy-on-write
+ * (openeuler.csdn.net PagedAttention notes, "机制 2：写时复制": a request that
+ * writes into a block it shares first gets its own copy).
+ *
+ *   block_pairs  device [num_pairs][2] int32: (source, destination) block ids.
+ *                Destinations must be distinct and must not be sources of the
+ *                same call (the pairs run concurrently).  A pair with an id
+ *                outside [0, num_blocks) is skipped and flagged
+ *                PKV_DEVERR_BLOCK_ID.
+ *   caches       as for pkv_reshape_and_cache, cache_dtype F16, BF16 or
+ *                FP8_E4M3; every (K and V) byte of the destination block
+ *                becomes the source block's.
+ * num_pairs == 0 launches nothing and returns PKV_OK.
+ */
+int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs, int num_pairs,
+                    int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                    pkv_dtype cache_dtype, uint32_t* device_errors, void* stream);
+
+/*
+ * Host block pool with prefix caching.  Sources: "第34讲 … vLLM 生产级系统架构
+ * 全景剖析与四重加速引擎", §1.2 (KVCacheManager.allocate_slots / free, BlockPool,
+ * FreeKVCacheBlockQueue), §2.2 (longest-prefix reuse with ref_cnt), §2.3
+ * (cached free blocks, LRU eviction); openeuler.csdn.net PagedAttention notes,
+ * "机制 2：写时复制" (fork, copy-on-write).
+ *
+ * Host memory only, no CUDA calls; not thread-safe (serialise calls on one
+ * pool and its requests).  The pool owns its requests' bookkeeping; a request
+ * must be freed before its pool is destroyed.
+ *
+ * Semantics:
+ *   - a fresh pool's free queue holds blocks 0, 1, ..., num_blocks - 1;
+ *     allocation takes the queue's head; a block whose reference count drops
+ *     to 0 joins the tail (a request releases its blocks last block first);
+ *   - a block is cached when it becomes full: it is registered under its
+ *     token prefix (every token from the request's start through the block's
+ *     last), unless that prefix is already registered to another block.  A
+ *     cached block keeps its registration at count 0 and is dropped from the
+ *     cache (evicted) only when allocation takes it from the queue;
+ *   - pkv_request_match_prefix reuses the longest run of cached blocks that
+ *     spells the start of the prompt, stopping before the block that holds
+ *     the prompt's last token (one token is always left to compute).
+ *     Reused blocks gain a reference and leave the free queue;
+ *   - pkv_request_append fills the last block first and takes new blocks
+ *     from the head.  If the last block is partial and shared (after a fork),
+ *     a private copy is made first: cow_out receives {source, copy} and the
+ *     caller copies the cache bytes (pkv_copy_blocks) before writing the new
+ *     tokens' K/V.  All or nothing: PKV_ERR_NO_BLOCKS leaves the pool and the
+ *     request unchanged.
+ */
+typedef struct pkv_block_pool pkv_block_pool;
+typedef struct pkv_request pkv_request;
+
+/* *out receives a new pool (NULL on error).  num_blocks >= 0, block_size > 0. */
+int pkv_block_pool_create(int32_t num_blocks, int32_t block_size, pkv_block_pool** out);
+void pkv_block_pool_destroy(pkv_block_pool* pool);
+/* Blocks in the free queue (cached or not); -1 for a NULL pool. */
+int32_t pkv_block_pool_num_free(const pkv_block_pool* pool);
+/* Registered (cached) blocks, in use or free; -1 for a NULL pool. */
+int32_t pkv_block_pool_num_cached(const pkv_block_pool* pool);
+/* Reference count / 1 if cached else 0; -1 for a bad pool or block id. */
+int32_t pkv_block_pool_ref_cnt(const pkv_block_pool* pool, int32_t block);
+int32_t pkv_block_pool_is_cached(const pkv_block_pool* pool, int32_t block);
+/* Copies up to max ids of the free queue, head first, into out (may be NULL
+ * when max is 0); returns the queue's length. */
+int32_t pkv_block_pool_queue(const pkv_block_pool* pool, int32_t* out, int32_t max);
+
+/* *out receives a new, empty request of the pool. */
+int pkv_request_create(pkv_block_pool* pool, pkv_request** out);
+/* On an empty request only (PKV_ERR_INVALID_ARG otherwise): reuse the cached
+ * prefix of tokens[0 .. num_tokens); *matched_out (may be NULL) receives the
+ * tokens covered, a multiple of block_size.  The caller then appends
+ * tokens[matched ..]. */
+int pkv_request_match_prefix(pkv_request* req, const int32_t* tokens, int32_t num_tokens,
+                             int32_t* matched_out);
+/* Appends num_tokens token ids.  slots_out (may be NULL) receives each new
+ * token's slot, physical_block * block_size + offset, for pkv_reshape_and_cache;
+ * cow_out (may be NULL) receives {source, copy} or {-1, -1}. */
+int pkv_request_append(pkv_request* req, const int32_t* token_ids, int32_t num_tokens,
+                       int64_t* slots_out, int32_t* cow_out);
+/* *out receives a request sharing every block of req (each gains a reference). */
+int pkv_request_fork(const pkv_request* req, pkv_request** out);
+/* Releases the request's blocks, last block first, and frees it. NULL is a no-op. */
+void pkv_request_free(pkv_request* req);
+/* Tokens held; -1 for NULL. */
+int32_t pkv_request_num_tokens(const pkv_request* req);
+/* Copies up to max block ids; returns the request's block count (-1 for NULL). */
+int32_t pkv_request_block_table(const pkv_request* req, int32_t* out, int32_t max);
+/* Host [num_reqs][max_blocks] block tables (entries past a request's blocks
+ * are 0) and context_lens (may be NULL) for a batch of requests, in the layout
+ * the attention calls take.  PKV_ERR_INVALID_ARG (nothing written) when a
+ * request holds more than max_blocks blocks. */
+int pkv_requests_block_tables(const pkv_request* const* reqs, int32_t num_reqs,
+                              int32_t max_blocks, int32_t* block_tables, int32_t* context_lens);
 
 /*
  * Synchronises `stream`, reads the device error word, clears it, and returns

@@ -27,6 +27,8 @@ __all__ = [
     "F16", "BF16", "FP8_E4M3", "PagedKVError", "library_path", "load", "reshape_and_cache",
     "decode_workspace_size", "prefill_workspace_size", "paged_attention_decode",
     "paged_attention_decode_noalloc", "paged_attention_prefill_chunk", "check_errors", "status_string", "version",
+    "paged_attention_prefill_tree", "cascade_workspace_size", "paged_attention_decode_cascade",
+    "copy_blocks", "BlockPool", "Request",
 ]
 
 F16, BF16, FP8_E4M3 = 0, 1, 2
@@ -92,6 +94,36 @@ def load():
                 [_P] * 8 + [_I] * 10 + [_F, _I, _I, _F, _F, _P, _SZ, _P, _P])
             lib.pkv_check_errors.restype = _I
             lib.pkv_check_errors.argtypes = [_P, _P, _P]
+            lib.pkv_copy_blocks.restype = _I
+            lib.pkv_copy_blocks.argtypes = [_P, _P, _P] + [_I] * 6 + [_P, _P]
+            _I32 = ctypes.c_int32
+            lib.pkv_block_pool_create.restype = _I
+            lib.pkv_block_pool_create.argtypes = [_I32, _I32, _P]
+            lib.pkv_block_pool_destroy.restype = None
+            lib.pkv_block_pool_destroy.argtypes = [_P]
+            for name in ("pkv_block_pool_num_free", "pkv_block_pool_num_cached",
+                         "pkv_request_num_tokens"):
+                getattr(lib, name).restype = _I32
+                getattr(lib, name).argtypes = [_P]
+            for name in ("pkv_block_pool_ref_cnt", "pkv_block_pool_is_cached"):
+                getattr(lib, name).restype = _I32
+                getattr(lib, name).argtypes = [_P, _I32]
+            lib.pkv_block_pool_queue.restype = _I32
+            lib.pkv_block_pool_queue.argtypes = [_P, _P, _I32]
+            lib.pkv_request_create.restype = _I
+            lib.pkv_request_create.argtypes = [_P, _P]
+            lib.pkv_request_match_prefix.restype = _I
+            lib.pkv_request_match_prefix.argtypes = [_P, _P, _I32, _P]
+            lib.pkv_request_append.restype = _I
+            lib.pkv_request_append.argtypes = [_P, _P, _I32, _P, _P]
+            lib.pkv_request_fork.restype = _I
+            lib.pkv_request_fork.argtypes = [_P, _P]
+            lib.pkv_request_free.restype = None
+            lib.pkv_request_free.argtypes = [_P]
+            lib.pkv_request_block_table.restype = _I32
+            lib.pkv_request_block_table.argtypes = [_P, _P, _I32]
+            lib.pkv_requests_block_tables.restype = _I
+            lib.pkv_requests_block_tables.argtypes = [_P, _I32, _I32, _P, _P]
             _lib = lib
     return _lib
 
@@ -301,6 +333,131 @@ def paged_attention_prefill_chunk(out, q, k_cache, v_cache, block_tables, contex
         wsb, _ptr(device_errors), _stream(stream))
     _check("pkv_paged_attention_prefill_chunk", rc)
     return out
+
+
+def copy_blocks(k_cache, v_cache, block_pairs, device_errors=None, stream=None):
+    """Copies whole blocks (block_pairs: [n, 2] int32 on the device, rows
+    (source, destination)) in both caches: the copy of copy-on-write."""
+    _need_cuda(k_cache, v_cache, block_pairs, device_errors)
+    nb, hkv, bs, d = k_cache.shape
+    n = block_pairs.shape[0] if block_pairs.dim() == 2 else block_pairs.numel() // 2
+    rc = load().pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_pairs), n, hkv, d, bs,
+                                nb, _dtype_code(k_cache), _ptr(device_errors), _stream(stream))
+    _check("pkv_copy_blocks", rc)
+
+
+def _host_i32(x):
+    import numpy as np
+    a = np.ascontiguousarray(x, dtype=np.int32)
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+class BlockPool:
+    """Host block pool with prefix caching (pkv_block_pool_*): hands out the
+    block tables and slot mappings the attention calls consume."""
+
+    def __init__(self, num_blocks: int, block_size: int = 16):
+        h = ctypes.c_void_p()
+        _check("pkv_block_pool_create",
+               load().pkv_block_pool_create(num_blocks, block_size, ctypes.byref(h)))
+        self.h, self.num_blocks, self.block_size = h, num_blocks, block_size
+        self._live = set()
+
+    def num_free(self) -> int:
+        return load().pkv_block_pool_num_free(self.h)
+
+    def num_cached(self) -> int:
+        return load().pkv_block_pool_num_cached(self.h)
+
+    def ref_cnt(self, block: int) -> int:
+        return load().pkv_block_pool_ref_cnt(self.h, block)
+
+    def is_cached(self, block: int) -> bool:
+        return load().pkv_block_pool_is_cached(self.h, block) == 1
+
+    def queue(self):
+        import numpy as np
+        out = np.empty(max(self.num_blocks, 1), dtype=np.int32)
+        n = load().pkv_block_pool_queue(self.h, out.ctypes.data_as(ctypes.c_void_p),
+                                        self.num_blocks)
+        return out[:n]
+
+    def request(self) -> "Request":
+        h = ctypes.c_void_p()
+        _check("pkv_request_create", load().pkv_request_create(self.h, ctypes.byref(h)))
+        return Request(self, h)
+
+    def block_tables(self, requests, max_blocks: int):
+        """([n, max_blocks] int32, [n] int32) numpy arrays for a batch of requests."""
+        import numpy as np
+        arr = (ctypes.c_void_p * max(len(requests), 1))(*[r.h.value for r in requests])
+        bt = np.empty((len(requests), max_blocks), dtype=np.int32)
+        cl = np.empty(len(requests), dtype=np.int32)
+        _check("pkv_requests_block_tables", load().pkv_requests_block_tables(
+            ctypes.cast(arr, ctypes.c_void_p), len(requests), max_blocks,
+            bt.ctypes.data_as(ctypes.c_void_p), cl.ctypes.data_as(ctypes.c_void_p)))
+        return bt, cl
+
+    def close(self):
+        for r in list(self._live):
+            r.free()
+        if self.h:
+            load().pkv_block_pool_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Request:
+    """One request's tokens and block table in a BlockPool."""
+
+    def __init__(self, pool: BlockPool, handle):
+        self.pool, self.h = pool, handle
+        pool._live.add(self)
+
+    def match_prefix(self, tokens) -> int:
+        a, p = _host_i32(tokens)
+        m = ctypes.c_int32()
+        _check("pkv_request_match_prefix",
+               load().pkv_request_match_prefix(self.h, p, len(a), ctypes.byref(m)))
+        return m.value
+
+    def append(self, token_ids):
+        """Returns (slots int64 numpy array, (source, copy) or None)."""
+        import numpy as np
+        a, p = _host_i32(token_ids)
+        slots = np.empty(max(len(a), 1), dtype=np.int64)
+        cow = np.empty(2, dtype=np.int32)
+        _check("pkv_request_append", load().pkv_request_append(
+            self.h, p, len(a), slots.ctypes.data_as(ctypes.c_void_p),
+            cow.ctypes.data_as(ctypes.c_void_p)))
+        return slots[:len(a)], (None if cow[0] < 0 else (int(cow[0]), int(cow[1])))
+
+    def fork(self) -> "Request":
+        h = ctypes.c_void_p()
+        _check("pkv_request_fork", load().pkv_request_fork(self.h, ctypes.byref(h)))
+        return Request(self.pool, h)
+
+    @property
+    def num_tokens(self) -> int:
+        return load().pkv_request_num_tokens(self.h)
+
+    def block_table(self):
+        import numpy as np
+        n = load().pkv_request_block_table(self.h, None, 0)
+        out = np.empty(max(n, 1), dtype=np.int32)
+        load().pkv_request_block_table(self.h, out.ctypes.data_as(ctypes.c_void_p), n)
+        return out[:n]
+
+    def free(self):
+        if self.h:
+            load().pkv_request_free(self.h)
+            self.h = None
+            self.pool._live.discard(self)
 
 
 def check_errors(device_errors, stream=None) -> int:

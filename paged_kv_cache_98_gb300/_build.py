@@ -1,4 +1,4 @@
-"""Builds libpagedkv.so in-tree from csrc/*.cu with nvcc for sm_103a.
+"""Builds libpagedkv.so in-tree from csrc/*.cu and csrc/*.cpp with nvcc for sm_103a.
 
 Each translation unit compiles in parallel into _build/, then nvcc links the
 shared library next to this file.  Rebuilds only what changed (by mtime,
@@ -45,12 +45,12 @@ def _stale(target: str, deps) -> bool:
 
 def build(verbose: bool = False, jobs: int | None = None, extra_flags=()) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     heads = _headers()
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(OUT_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         if _stale(obj, [src] + heads):
             cmd = [cc] + NVCC_FLAGS + list(extra_flags) + ["-c", src, "-o", obj]
             if verbose:

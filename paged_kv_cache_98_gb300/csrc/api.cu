@@ -125,6 +125,7 @@ const char* pkv_status_string(int status) {
     case PKV_ERR_CUDA: return "CUDA error";
     case PKV_ERR_DEVICE: return "device-side check failed";
     case PKV_ERR_TIMEOUT: return "device-side wait timed out";
+    case PKV_ERR_NO_BLOCKS: return "block pool exhausted";
     default: return "unknown status";
   }
 }

@@ -389,5 +389,19 @@ def values_device(w: Workload, device):
     return k, v, q
 
 
+def token_kv(seed: int, tokens, positions, Hkv: int, D: int, dtype: int, vocab: int = 1024,
+             max_pos: int = 8192):
+    """(k, v) bits [n, Hkv, D] for tokens at positions: per-token and
+    per-position N(0,1) embeddings (fp32, from PCG64(seed)) summed and rounded,
+    so equal (token, position) pairs always give equal K/V, as a cached prefix
+    block must."""
+    r = rng(seed)
+    et = r.standard_normal(size=(2, vocab, Hkv, D), dtype=np.float32)
+    ep = r.standard_normal(size=(2, max_pos, Hkv, D), dtype=np.float32)
+    t = np.asarray(tokens, np.int64) % vocab
+    p = np.asarray(positions, np.int64)
+    return (_round_bits(et[0, t] + ep[0, p], dtype), _round_bits(et[1, t] + ep[1, p], dtype))
+
+
 def query_start_loc(q_lens) -> np.ndarray:
     return np.concatenate([[0], np.cumsum(np.asarray(q_lens, np.int64))]).astype(np.int32)
