@@ -121,12 +121,14 @@ struct Item {
 
 // Key chunks of a sequence: all its key tiles in one item, or (shared-prefix
 // mode) prefix_chunk keys per item.
+template <bool kAlt>
 __device__ __forceinline__ int key_chunks(const AttnParams& p, int ctx) {
-  if (p.prefix_chunk <= 0) return 1;
+  if (!kAlt || p.prefix_chunk <= 0) return 1;
   const int tiles = (ctx + kTileKeys - 1) / kTileKeys, per = p.prefix_chunk / kTileKeys;
   return (tiles + per - 1) / per;
 }
 
+template <bool kAlt>
 __device__ __forceinline__ bool next_item(const AttnParams& p, const Smem& sm, int& idx,
                                           int total, Item& it) {
   if (idx >= total) return false;
@@ -146,21 +148,21 @@ __device__ __forceinline__ bool next_item(const AttnParams& p, const Smem& sm, i
   it.ctx = sm.seq_ctx[lo];
   it.q0 = sm.seq_q0[lo];
   it.trow = p.seq_rows ? __ldg(p.seq_rows + lo) : lo;
-  const int nch = key_chunks(p, it.ctx);
+  const int nch = key_chunks<kAlt>(p, it.ctx);
   const int npairs = (sm.seq_start[lo + 1] - sm.seq_start[lo]) / nch;
   const int in_seq = pair - sm.seq_start[lo];
   const int mp = npairs - 1 - in_seq / nch;  // longest pairs first
-  const bool alt = p.partial_out != 0;       // one query tile, alternating key tiles
+  constexpr bool alt = kAlt;  // one query tile, alternating key tiles
   it.chunk = in_seq % nch;
-  it.kt0 = p.prefix_chunk > 0 ? it.chunk * (p.prefix_chunk / kTileKeys) : 0;
-  const int kt1 = p.prefix_chunk > 0 ? it.kt0 + p.prefix_chunk / kTileKeys : INT_MAX;
+  it.kt0 = kAlt && p.prefix_chunk > 0 ? it.chunk * (p.prefix_chunk / kTileKeys) : 0;
+  const int kt1 = kAlt && p.prefix_chunk > 0 ? it.kt0 + p.prefix_chunk / kTileKeys : INT_MAX;
   it.nk = 0;
 #pragma unroll
   for (int x = 0; x < 2; ++x) {
     it.t0[x] = (alt ? mp : 2 * mp + x) * rpt;
     it.nt[x] = max(0, min(rpt, qlen - it.t0[x]));
-    it.pos0[x] = p.non_causal ? it.ctx - 1 : it.ctx - qlen + it.t0[x];
-    const int last = p.non_causal ? it.pos0[x] : it.pos0[x] + it.nt[x] - 1;
+    it.pos0[x] = kAlt ? it.ctx - 1 : it.ctx - qlen + it.t0[x];
+    const int last = kAlt ? it.pos0[x] : it.pos0[x] + it.nt[x] - 1;
     it.nkt[x] = it.nt[x] > 0 ? min(kt1, last / kTileKeys + 1) : 0;
     it.nk = max(it.nk, it.nkt[x]);
   }
@@ -242,8 +244,9 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
-// kTree: draft-tree mode (per-row ancestor masks over the chunk's keys)
-template <class QT, bool kTree>
+// kTree: draft-tree mode (per-row ancestor masks over the chunk's keys);
+// kAlt: shared-prefix mode (non-causal, key chunks, partial outputs)
+template <class QT, bool kTree, bool kAlt>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
@@ -299,11 +302,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q0 = __ldg(p.query_start_loc + sq);
         int qlen = __ldg(p.query_start_loc + sq + 1) - q0;
         int ctx = __ldg(p.context_lens + (p.seq_rows ? __ldg(p.seq_rows + sq) : sq));
-        if (ctx < 0 || ctx > cap || qlen < 0 || (!p.non_causal && qlen > ctx) || q0 < 0 ||
+        if (ctx < 0 || ctx > cap || qlen < 0 || (!kAlt && qlen > ctx) || q0 < 0 ||
             q0 + qlen > p.num_rows || (kTree && qlen > 64)) {
           flag_error(p.errors, PKV_DEVERR_CONTEXT);
           ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
-          qlen = qlen < 0 ? 0 : (!p.non_causal && qlen > ctx ? ctx : qlen);
+          qlen = qlen < 0 ? 0 : (!kAlt && qlen > ctx ? ctx : qlen);
           if (kTree && qlen > 64) qlen = 64;  // the mask covers 64 chunk keys
           if (q0 < 0 || q0 + qlen > p.num_rows) qlen = 0;
         }
@@ -311,8 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm.seq_ctx[sq] = ctx;
         sm.seq_q0[sq] = q0;
         const int tiles = (qlen * g + kRowsM - 1) / kRowsM;
-        const int units = p.partial_out ? tiles : (tiles + 1) / 2;
-        local += ctx > 0 ? units * key_chunks(p, ctx) : 0;
+        const int units = kAlt ? tiles : (tiles + 1) / 2;
+        local += ctx > 0 ? units * key_chunks<kAlt>(p, ctx) : 0;
       }
     }
     int incl = local;
@@ -332,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm.seq_start[sq] = run;
         const int c = sm.seq_ctx[sq];
         const int tiles = (sm.seq_qlen[sq] * g + kRowsM - 1) / kRowsM;
-        run += c > 0 ? (p.partial_out ? tiles : (tiles + 1) / 2) * key_chunks(p, c) : 0;
+        run += c > 0 ? (kAlt ? tiles : (tiles + 1) / 2) * key_chunks<kAlt>(p, c) : 0;
       }
     }
     if (tid == kThreads - 1) sm.seq_start[S] = base + incl;
@@ -350,8 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pw = warp - 9;
     const int mine = (8 - pw + kProducers - 1) / kProducers;  // blocks per tile: 3, 3, 2
     const bool my_lane = (lane & 7) % kProducers == pw;
-    const bool alt = p.partial_out != 0;  // shared-prefix mode
-    const int nst = alt ? kMaxStages : kStages;
+    constexpr bool alt = kAlt;  // shared-prefix mode
+    constexpr int nst = alt ? kMaxStages : kStages;
     uint8_t* const ring = &sm.ring[0][0];  // stage 4 (shared-prefix mode) is q[0]
     int idx = blockIdx.x;
     uint32_t pos = 0;
@@ -417,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++ntail;
       return true;
     };
-    while (ok && next_item(p, sm, idx, total, x)) {
+    while (ok && next_item<kAlt>(p, sm, idx, total, x)) {
       bool good = true;
       if (pw == 0 && lane == 0) {
         if (nitem >= 1) good = wait_bar(&sm.q_empty, (nitem - 1) & 1, abort);
@@ -490,8 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       Item x;
       const uint32_t qaddr[2] = {smem_u32(&sm.q[0][0]), smem_u32(&sm.q[1][0])};
       const uint32_t taddr = smem_u32(&sm.tail[0]);
-      const bool alt = p.partial_out != 0;  // shared-prefix mode
-      const int nst = alt ? kMaxStages : kStages;
+      constexpr bool alt = kAlt;  // shared-prefix mode
+      constexpr int nst = alt ? kMaxStages : kStages;
       auto acquire = [&](int& st) -> bool {
         st = pos % nst;
         const bool r = wait_bar(&sm.full[st], (pos / nst) & 1, abort);
@@ -580,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
-      while (ok && next_item(p, sm, idx, total, x)) {
+      while (ok && next_item<kAlt>(p, sm, idx, total, x)) {
         const bool ha = x.last[0] >= 0;
         const bool hb = x.last[1] >= 0;
         int kst = 0, vst = 0;
@@ -645,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ns = 0, nit = 0;  // S tiles and items of this query tile
     bool ok = true;
     Item x;
-    while (ok && next_item(p, sm, idx, total, x)) {
+    while (ok && next_item<kAlt>(p, sm, idx, total, x)) {
       const int tok = tid / g;  // token within the tile
       // rows past the tile's tokens compute on whatever Q holds there; their
       // output is never stored
@@ -656,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (x.last[qt] < 0) {
         // no key tile for this warpgroup here (no tile b, or a one-tile chunk in
         // shared-prefix mode, whose empty partial then weighs nothing)
-        if (p.partial_out && valid && x.nt[qt] > 0 && slot < p.max_parts) {
+        if (kAlt && valid && x.nt[qt] > 0 && slot < p.max_parts) {
           p.lse[head * p.max_parts + slot] = -INFINITY;
           float4* z = reinterpret_cast<float4*>(p.o_part + (head * p.max_parts + slot) * kD);
 #pragma unroll 4
@@ -664,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;
       }
-      const int qpos = x.pos0[qt] + (p.non_causal ? 0 : tok);
+      const int qpos = x.pos0[qt] + (kAlt ? 0 : tok);
       // draft-tree mode: the row's visible chunk keys, from the chunk's first position
       const int cbase = x.pos0[qt] - x.t0[qt];
       const uint64_t tmask =
@@ -798,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       OutT* orow = static_cast<OutT*>(p.out) + head * kD;
       // shared-prefix mode: the normalised partial and its log-sum-exp (base 2,
       // scaled units), in the warpgroup's slot of the chunk
-      const bool part = p.partial_out && slot < p.max_parts;
+      const bool part = kAlt && slot < p.max_parts;
       float* prow = part ? p.o_part + (head * p.max_parts + slot) * kD : nullptr;
       if (part && valid) p.lse[head * p.max_parts + slot] = m_run + log2f(l);
 #pragma unroll 1
@@ -859,14 +862,16 @@ int launch_typed(const AttnParams& p, int total_q, cudaStream_t stream) {
                 "swizzled buffers must start on 1024-byte boundaries");
   static_assert(offsetof(Smem, q) == offsetof(Smem, ring) + kStages * kTileBytes,
                 "q[0] is the ring's fifth stage in shared-prefix mode");
-  const bool tree = p.tree_mask != nullptr;
-  auto kern = tree ? prefill_tc_kernel<QT, true> : prefill_tc_kernel<QT, false>;
-  static bool configured[2] = {false, false};
-  if (!configured[tree]) {
+  const int mode = p.tree_mask != nullptr ? 1 : (p.partial_out ? 2 : 0);
+  auto kern = mode == 1   ? prefill_tc_kernel<QT, true, false>
+              : mode == 2 ? prefill_tc_kernel<QT, false, true>
+                          : prefill_tc_kernel<QT, false, false>;
+  static bool configured[3] = {false, false, false};
+  if (!configured[mode]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return PKV_ERR_CUDA;
-    configured[tree] = true;
+    configured[mode] = true;
   }
   // an upper bound of the items: every sequence's tile pairs, times the KV heads
   const long long tiles = ((long long)total_q * p.group + (long long)p.num_seqs * (kRowsM - 1)) /
