@@ -46,6 +46,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-also", action="store_true", help="skip the other workloads")
+    ap.add_argument("--mixed-entry", default="separate", choices=["separate", "fused"],
+                    help="a batch with decode rows and chunks: separate decode and prefill "
+                         "calls, or one pkv_paged_attention_mixed call")
     ap.add_argument("--decode-entry", default="plain", choices=["plain", "cascade"],
                     help="decode through pkv_paged_attention_decode or, reading each shared "
                          "prompt block once per group, pkv_paged_attention_decode_cascade")
@@ -171,7 +174,7 @@ class GpuStep:
     """Device-resident state of one workload and its step (cache write, decode
     attention, and prefill-chunk attention when the workload has chunks)."""
 
-    def __init__(self, w, dev, cascade=False):
+    def __init__(self, w, dev, cascade=False, fused=False):
         import numpy as np
         import torch
 
@@ -224,6 +227,20 @@ class GpuStep:
             nb = pkv.prefill_workspace_size(self.q_pre.shape[0], H, D, self.max_ctx_pre,
                                             self.max_q_pre)
             self.ws_pre = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+        self.has_mixed = len(self.dec) > 0 and len(self.pre) > 0
+        self.fused = fused and self.has_mixed
+        if self.has_mixed:
+            # one call over the whole batch (the workload lists its decode rows first)
+            nd = len(self.dec)
+            assert np.array_equal(self.dec, np.arange(nd))
+            self.q_all = q.contiguous()
+            self.bt_all = torch.from_numpy(np.ascontiguousarray(w.block_tables)).to(dev)
+            self.cl_all = torch.from_numpy(np.ascontiguousarray(w.context_lens)).to(dev)
+            self.qsl_all = torch.from_numpy(qsl).to(dev)
+            self.out_all = torch.empty_like(self.q_all)
+            self.max_ctx_all = int(w.context_lens.max())
+            nb = pkv.mixed_workspace_size(nd, self.q_all.shape[0], H, D, self.max_ctx_all)
+            self.ws_all = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
         self.cascade = cascade
         if cascade:
             gs, pre = w.cascade_groups()
@@ -273,6 +290,8 @@ class GpuStep:
 
     def launches_per_step(self) -> int:
         n = 1  # cache write
+        if self.fused:
+            return n + 1 + (1 if self.parts > 1 else 0)  # fused attention, decode merge
         if len(self.dec) and self.cascade:
             n += 3  # shared-prefix pass, own-keys decode, merge
         elif len(self.dec):
@@ -285,7 +304,41 @@ class GpuStep:
         self.pkv.reshape_and_cache(self.k_new, self.v_new, self.kc, self.vc, self.slots, self.ks,
                                    self.vs, device_errors=self.err)
 
+    def mixed(self):
+        self.pkv.paged_attention_mixed(
+            self.out_all, self.q_all, self.kc, self.vc, self.bt_all, self.cl_all, self.qsl_all,
+            len(self.dec), self.w.scale, max_q_len=self.max_q_pre,
+            max_context_len=self.max_ctx_all, workspace=self.ws_all, device_errors=self.err)
+
+    def fused_timed(self, steps: int, warmup: int) -> float:
+        """Mean CUDA-event time (ms) of the whole batch's attention in one
+        pkv_paged_attention_mixed call; its output is checked against the
+        separate decode and prefill calls' (they run the same arithmetic)."""
+        import torch
+        fused, self.fused = self.fused, False
+        for _ in range(warmup):
+            self.mixed()
+        self.decode()
+        self.prefill()
+        self.fused = fused
+        torch.cuda.synchronize(self.dev)
+        nd = len(self.dec)
+        if not (torch.equal(self.out_all[:nd], self.out) and
+                torch.equal(self.out_all[nd:], self.out_pre)):
+            raise RuntimeError("fused mixed-batch attention disagrees with the separate calls")
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(steps):
+            self.mixed()
+        t1.record()
+        torch.cuda.synchronize(self.dev)
+        return t0.elapsed_time(t1) / steps
+
     def decode(self):
+        if self.fused:
+            self.mixed()
+            return
         if len(self.dec) and self.cascade:
             self.pkv.paged_attention_decode_cascade(
                 self.out, self.q_dec, self.kc, self.vc, self.bt, self.cl, self.casc_gs,
@@ -298,7 +351,7 @@ class GpuStep:
                 device_errors=self.err)
 
     def prefill(self):
-        if len(self.pre):
+        if len(self.pre) and not self.fused:
             self.pkv.paged_attention_prefill_chunk(
                 self.out_pre, self.q_pre, self.kc, self.vc, self.bt_pre, self.cl_pre, self.qsl_pre,
                 self.w.scale, max_q_len=self.max_q_pre, max_context_len=self.max_ctx_pre,
@@ -348,6 +401,10 @@ class GpuStep:
         import torch
         host = {}
         names = ("k_new", "v_new", "slots", "q_dec", "bt", "cl")
+        if len(self.pre):
+            names += ("q_pre", "bt_pre", "cl_pre", "qsl_pre")
+        if self.fused:
+            names = ("k_new", "v_new", "slots", "q_all", "bt_all", "cl_all", "qsl_all")
         if self.cascade:
             names += ("casc_gs", "casc_pre")
         for name in names:
@@ -355,7 +412,8 @@ class GpuStep:
             h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
             h.copy_(t)
             host[name] = h
-        out_h = torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True)
+        res = self.out_all if self.fused else self.out
+        out_h = torch.empty(res.shape, dtype=res.dtype, pin_memory=True)
         h2d = sum(h.numel() * h.element_size() for h in host.values())
         d2h = out_h.numel() * out_h.element_size()
 
@@ -363,7 +421,7 @@ class GpuStep:
             for name, h in host.items():
                 getattr(self, name).copy_(h, non_blocking=True)
             self.step()
-            out_h.copy_(self.out, non_blocking=True)
+            out_h.copy_(res, non_blocking=True)
 
         for _ in range(warmup):
             one()
@@ -491,7 +549,7 @@ def main():
 
     w = workloads.NAMED[args.workload]()
     cascade = args.decode_entry == "cascade"
-    st = GpuStep(w, dev, cascade=cascade)
+    st = GpuStep(w, dev, cascade=cascade, fused=args.mixed_entry == "fused")
     sampler = ClockSampler(local).start()
     time.sleep(0.3)
     res = st.timed(args.steps, args.warmup, barrier)
@@ -533,7 +591,7 @@ def main():
             "num_seqs": w.num_seqs, "context": int(w.context_lens.max()),
             "num_heads": w.num_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
             "block_size": 16, "partition": 512, "pool_blocks": w.num_blocks,
-            "decode_entry": args.decode_entry,
+            "decode_entry": args.decode_entry, "mixed_entry": args.mixed_entry,
             "kv_bytes_per_step": kv_bytes,
             "l2": f"inputs larger than L2: {kv_bytes / 1e9:.2f} GB of K/V read per step "
                   "vs 129 MB L2",
@@ -606,6 +664,12 @@ def other_workloads(dev, peak, barrier):
             d["cascade_GBps_logical"] = round(kvb / (cms * 1e-3) / 1e9, 1)
             d["cascade_GBps_unique"] = round(ub / (cms * 1e-3) / 1e9, 1)
             d["cascade_speedup"] = round(res["decode_ms"] / cms, 3)
+        if name == "mixed":
+            # the same batch's attention in one fused call
+            fms = st.fused_timed(steps, 5)
+            d["fused_attention_ms"] = round(fms, 5)
+            d["separate_attention_ms"] = round(res["decode_ms"] + res["prefill_ms"], 5)
+            d["fused_speedup"] = round((res["decode_ms"] + res["prefill_ms"]) / fms, 3)
         if len(w.prefill_ids()):
             flops = 0
             for s in w.prefill_ids():

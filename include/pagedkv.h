@@ -291,6 +291,43 @@ int pkv_paged_attention_decode_cascade(void* out, const void* q, const void* k_c
                                        uint32_t* device_errors, void* stream);
 
 /*
+ * A mixed batch in one launch: the step's single-token decode rows and its
+ * prefill chunks ("第32讲 … Prefill vs Decode …", §5.4 chunked prefill: one
+ * batch carries the running decodes and slices of new prompts).  The result
+ * equals pkv_paged_attention_decode on the decode rows plus
+ * pkv_paged_attention_prefill_chunk on the chunks; with 16-bit caches,
+ * head_dim 128 and num_heads / num_kv_heads in 2..8, one kernel does both
+ * (its CTAs split between the two kinds of work), followed by the
+ * partition merge of the decode rows when their contexts exceed 512 tokens.
+ * Other shapes run the two calls one after the other.
+ *
+ *   sequences     [0, num_decode) are decode rows: query row s, and
+ *                 query_start_loc[s] = s for s <= num_decode;
+ *                 [num_decode, num_seqs) are chunks with query rows
+ *                 query_start_loc[s] .. query_start_loc[s + 1] - 1.
+ *   block_tables,
+ *   context_lens  one row / entry per sequence, in the same order.
+ *   max_context_len  bounds every context_lens entry; max_q_len the chunks.
+ *   prefill_ctas  0: the kernel divides the SMs between chunks and decode
+ *                 rows from their lengths; > 0: the chunks get that many CTAs
+ *                 (clamped to [1, SMs - 1]).
+ *   workspace     at least pkv_mixed_workspace_size bytes, 256-byte aligned
+ *                 (NULL when that is 0).
+ * Other arguments as for pkv_paged_attention_prefill_chunk.
+ */
+size_t pkv_mixed_workspace_size(int num_decode, int total_q, int num_heads, int head_dim,
+                                int max_context_len);
+int pkv_paged_attention_mixed(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, const int32_t* context_lens,
+                              const int32_t* query_start_loc, int num_decode, int num_seqs,
+                              int total_q, int max_q_len, int num_heads, int num_kv_heads,
+                              int head_dim, int block_size, int max_blocks_per_seq,
+                              int num_blocks, int max_context_len, float scale,
+                              pkv_dtype q_dtype, pkv_dtype kv_dtype, float k_scale,
+                              float v_scale, int prefill_ctas, void* workspace,
+                              size_t workspace_bytes, uint32_t* device_errors, void* stream);
+
+/*
  * Whole-block copies in both caches: the device half of copy-on-write
  * (openeuler.csdn.net PagedAttention notes, "机制 2：写时复制": a request that
  * writes into a block it shares first gets its own copy).

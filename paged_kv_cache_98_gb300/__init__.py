@@ -28,7 +28,7 @@ __all__ = [
     "decode_workspace_size", "prefill_workspace_size", "paged_attention_decode",
     "paged_attention_decode_noalloc", "paged_attention_prefill_chunk", "check_errors", "status_string", "version",
     "paged_attention_prefill_tree", "cascade_workspace_size", "paged_attention_decode_cascade",
-    "copy_blocks", "BlockPool", "Request",
+    "copy_blocks", "BlockPool", "Request", "mixed_workspace_size", "paged_attention_mixed",
 ]
 
 F16, BF16, FP8_E4M3 = 0, 1, 2
@@ -94,6 +94,11 @@ def load():
                 [_P] * 8 + [_I] * 10 + [_F, _I, _I, _F, _F, _P, _SZ, _P, _P])
             lib.pkv_check_errors.restype = _I
             lib.pkv_check_errors.argtypes = [_P, _P, _P]
+            lib.pkv_mixed_workspace_size.restype = _SZ
+            lib.pkv_mixed_workspace_size.argtypes = [_I] * 5
+            lib.pkv_paged_attention_mixed.restype = _I
+            lib.pkv_paged_attention_mixed.argtypes = (
+                [_P] * 7 + [_I] * 11 + [_F, _I, _I, _F, _F, _I, _P, _SZ, _P, _P])
             lib.pkv_copy_blocks.restype = _I
             lib.pkv_copy_blocks.argtypes = [_P, _P, _P] + [_I] * 6 + [_P, _P]
             _I32 = ctypes.c_int32
@@ -332,6 +337,39 @@ def paged_attention_prefill_chunk(out, q, k_cache, v_cache, block_tables, contex
         max_context_len, scale, _dtype_code(q), _dtype_code(k_cache), k_scale, v_scale, _ptr(ws),
         wsb, _ptr(device_errors), _stream(stream))
     _check("pkv_paged_attention_prefill_chunk", rc)
+    return out
+
+
+def mixed_workspace_size(num_decode: int, total_q: int, num_heads: int, head_dim: int,
+                         max_context_len: int) -> int:
+    return int(load().pkv_mixed_workspace_size(num_decode, total_q, num_heads, head_dim,
+                                                max_context_len))
+
+
+def paged_attention_mixed(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc,
+                          num_decode: int, scale: float, max_q_len: int | None = None,
+                          max_context_len: int | None = None, k_scale: float = 1.0,
+                          v_scale: float = 1.0, prefill_ctas: int = 0, workspace=None,
+                          device_errors=None, stream=None):
+    """One step's decode rows (the first num_decode sequences, one query row
+    each) and prefill chunks (the rest) in one call; see pkv_paged_attention_mixed."""
+    _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc,
+               device_errors)
+    TQ, H, D = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    S = context_lens.shape[0]
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if S else 0
+    if max_q_len is None:
+        max_q_len = int((query_start_loc[1:] - query_start_loc[:-1]).max().item()) if S else 0
+    need = mixed_workspace_size(num_decode, TQ, H, D, max_context_len)
+    ws, wsb = _workspace(need, workspace, q.device)
+    rc = load().pkv_paged_attention_mixed(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        _ptr(query_start_loc), num_decode, S, TQ, max_q_len, H, hkv, D, bs,
+        block_tables.shape[1], nb, max_context_len, scale, _dtype_code(q), _dtype_code(k_cache),
+        k_scale, v_scale, prefill_ctas, _ptr(ws), wsb, _ptr(device_errors), _stream(stream))
+    _check("pkv_paged_attention_mixed", rc)
     return out
 
 

@@ -304,6 +304,102 @@ int pkv_paged_attention_prefill_tree(void* out, const void* q, const void* k_cac
   return pkv::launch_prefill_tc(p, q_dtype, total_q, static_cast<cudaStream_t>(stream));
 }
 
+size_t pkv_mixed_workspace_size(int num_decode, int total_q, int num_heads, int head_dim,
+                                int max_context_len) {
+  const size_t d = pkv_decode_workspace_size(num_decode, num_heads, head_dim, max_context_len, 0);
+  const size_t p =
+      pkv_prefill_workspace_size(total_q - num_decode, num_heads, head_dim, max_context_len, 0);
+  return d > p ? d : p;
+}
+
+int pkv_paged_attention_mixed(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, const int32_t* context_lens,
+                              const int32_t* query_start_loc, int num_decode, int num_seqs,
+                              int total_q, int max_q_len, int num_heads, int num_kv_heads,
+                              int head_dim, int block_size, int max_blocks_per_seq,
+                              int num_blocks, int max_context_len, float scale,
+                              pkv_dtype q_dtype, pkv_dtype kv_dtype, float k_scale,
+                              float v_scale, int prefill_ctas, void* workspace,
+                              size_t workspace_bytes, uint32_t* device_errors, void* stream) {
+  int rc = check_attention_args(out, q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                num_heads, num_kv_heads, head_dim, block_size,
+                                max_blocks_per_seq, num_blocks, max_context_len, scale, q_dtype,
+                                kv_dtype, k_scale, v_scale);
+  if (rc != PKV_OK) return rc;
+  if (!query_start_loc || num_decode < 0 || num_decode > num_seqs || total_q < num_decode ||
+      max_q_len < 0 || prefill_ctas < 0)
+    return PKV_ERR_INVALID_ARG;
+  const int num_chunks = num_seqs - num_decode;
+  // the chunks' block-table rows, lengths and offsets follow the decode rows'
+  const int32_t* bt_pre = block_tables + (size_t)num_decode * max_blocks_per_seq;
+  if (num_chunks == 0 || total_q == num_decode)
+    return pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
+                                      num_decode, num_heads, num_kv_heads, head_dim, block_size,
+                                      max_blocks_per_seq, num_blocks, max_context_len, scale,
+                                      q_dtype, kv_dtype, k_scale, v_scale, 0, workspace,
+                                      workspace_bytes, device_errors, stream);
+  if (num_decode == 0)
+    return pkv_paged_attention_prefill_chunk(
+        out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc, num_seqs, total_q,
+        max_q_len, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+        max_context_len, scale, q_dtype, kv_dtype, k_scale, v_scale, workspace, workspace_bytes,
+        device_errors, stream);
+  pkv::AttnParams pd{};
+  pd.out = out;
+  pd.q = q;
+  pd.k_cache = static_cast<const uint8_t*>(k_cache);
+  pd.v_cache = static_cast<const uint8_t*>(v_cache);
+  pd.block_tables = block_tables;
+  pd.context_lens = context_lens;
+  pd.num_seqs = pd.num_rows = num_decode;
+  pd.num_heads = num_heads;
+  pd.num_kv_heads = num_kv_heads;
+  pd.group = num_heads / num_kv_heads;
+  pd.max_blocks_per_seq = max_blocks_per_seq;
+  pd.num_blocks = num_blocks;
+  pd.partition = kDefaultPartition;
+  pd.max_parts = parts_for(max_context_len, kDefaultPartition);
+  if (pd.max_parts > 16384) return PKV_ERR_UNSUPPORTED;
+  pd.errors = device_errors;
+  pkv::AttnParams pp = pd;
+  pp.block_tables = bt_pre;
+  pp.context_lens = context_lens + num_decode;
+  pp.query_start_loc = query_start_loc + num_decode;
+  pp.num_seqs = num_chunks;
+  pp.num_rows = total_q;
+  const bool fused = pkv::tc_mixed_supported(pd, pp, q_dtype, kv_dtype, head_dim);
+  if (!fused) {
+    // the two launches the fused kernel replaces, sharing the workspace in stream order
+    rc = pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
+                                    num_decode, num_heads, num_kv_heads, head_dim, block_size,
+                                    max_blocks_per_seq, num_blocks, max_context_len, scale,
+                                    q_dtype, kv_dtype, k_scale, v_scale, 0, workspace,
+                                    workspace_bytes, device_errors, stream);
+    if (rc != PKV_OK) return rc;
+    return pkv_paged_attention_prefill_chunk(
+        out, q, k_cache, v_cache, bt_pre, context_lens + num_decode, query_start_loc + num_decode,
+        num_chunks, total_q, max_q_len, num_heads, num_kv_heads, head_dim, block_size,
+        max_blocks_per_seq, num_blocks, max_context_len, scale, q_dtype, kv_dtype, k_scale,
+        v_scale, workspace, workspace_bytes, device_errors, stream);
+  }
+  const size_t need = split_workspace((size_t)num_decode, num_heads, head_dim, pd.max_parts);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return PKV_ERR_INVALID_ARG;
+    const size_t heads = (size_t)num_decode * num_heads * pd.max_parts;
+    pd.lse = static_cast<float*>(workspace);
+    pd.o_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                         round_up(heads * sizeof(float), 256));
+  }
+  pd.q_scale = pp.q_scale = scale * pkv::kLog2e;
+  pd.v_scale = pp.v_scale = 1.0f;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  rc = pkv::launch_mixed_tc(pd, pp, q_dtype, total_q, prefill_ctas, st);
+  if (rc != PKV_OK) return rc;
+  if (pd.max_parts > 1) rc = pkv::launch_lse_merge(pd, q_dtype, head_dim, st);
+  return rc;
+}
+
 size_t pkv_cascade_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len,
                                   int max_prefix_len) {
   if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||

@@ -76,6 +76,15 @@ int launch_paged_decode_tc(const AttnParams& p, int q_dtype, int kv_dtype, cudaS
 bool tc_prefill_supported(const AttnParams& p, int q_dtype, int kv_dtype, int head_dim);
 int launch_prefill_tc(const AttnParams& p, int q_dtype, int total_q, cudaStream_t stream);
 
+// One launch for a mixed batch: pd describes the decode rows (as for
+// launch_paged_decode_tc), pp the prefill chunks (as for launch_prefill_tc);
+// the CTAs are split between the two (prefill_ctas > 0 fixes the chunks'
+// share, 0 lets the kernel weigh the batch).  16-bit caches, group <= 8.
+bool tc_mixed_supported(const AttnParams& pd, const AttnParams& pp, int q_dtype, int kv_dtype,
+                        int head_dim);
+int launch_mixed_tc(const AttnParams& pd, const AttnParams& pp, int q_dtype, int total_q,
+                    int prefill_ctas, cudaStream_t stream);
+
 // Host helpers (host_util.cu).
 bool tmap_available();
 bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, bool bf16, uint32_t box_rows);

@@ -158,3 +158,30 @@ def test_tree_argument_validation(lib):
     long[10] = 65  # max_q_len above 64
     assert f(*long) == -1
     assert f(*args[:8], 0, *args[9:]) == 0  # no sequences
+
+
+def test_mixed_argument_validation(lib):
+    f = lib.pkv_paged_attention_mixed
+    # out q k v tables lens qsl | decode seqs total_q max_q H Hkv D bs MB NB max_ctx | scale
+    # dtypes scales | prefill_ctas workspace bytes errors stream
+    args = [256, 256, 512, 512, 1024, 2048, 4096, 2, 4, 40, 16, 8, 2, 128, 16, 4, 8, 64, 0.1,
+            1, 1, 1.0, 1.0, 0, None, 0, None, None]
+
+    def call(**over):
+        a = list(args)
+        for i, v in over.items():
+            a[int(i[1:])] = v
+        return f(*a)
+
+    assert call(a6=None) == -1       # no query_start_loc
+    assert call(a7=5) == -1          # more decode rows than sequences
+    assert call(a9=1) == -1          # fewer query rows than decode rows
+    assert call(a23=-1) == -1        # negative CTA share
+    assert call(a7=0, a8=0, a9=0) == 0  # empty batch: nothing launched
+
+
+def test_mixed_workspace_size(lib):
+    # the larger of the decode rows' and the chunks' needs
+    d = pkv.decode_workspace_size(32, 32, 128, 8192)
+    p = pkv.prefill_workspace_size(2048, 32, 128, 8192, 512)
+    assert pkv.mixed_workspace_size(32, 2080, 32, 128, 8192) == max(d, p)

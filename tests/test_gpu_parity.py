@@ -175,6 +175,19 @@ def test_prefill_chunks(g):
     run_case(w)
 
 
+@pytest.mark.parametrize("seed,g,dt", [(0, 4, BF16), (1, 8, F16), (2, 2, BF16), (3, 4, F16)])
+def test_prefill_from_position_zero(seed, g, dt):
+    """Whole prompts as chunks (no prior context): the first rows see one to a
+    few dozen keys, where 16-bit softmax weights alone would not meet the
+    tolerance; chunks shorter and longer than the recomputed rows, and one
+    starting just inside them."""
+    qlen = [5, 31, 32, 33, 200, 17]
+    ctx = [5, 31, 32, 33, 200, 17 + 20]
+    w = workloads.independent("prefill-from-0", 3100 + seed, ctx, 4 * g, 4, 128, dt, dt,
+                              q_lens=qlen)
+    run_case(w)
+
+
 def test_mixed_small():
     w = workloads.mixed(seed=5, num_decode=6, num_prefill=2, chunk=96, prior=200)
     run_case(w)
