@@ -190,6 +190,91 @@ __device__ __forceinline__ bool next_item(const AttnParams& p, const SM& sm, int
   return true;
 }
 
+// Rows that see at most this many keys are recomputed in fp32 on the CUDA
+// cores after the main loop: with so few keys the rounding of the softmax
+// weights to the MMA's 16-bit (or E4M3) input does not average out.
+constexpr int kFewKeys = 32;
+
+// Decode rows with at most kFewKeys keys (one partition, no shared prefix):
+// the plain online softmax over the keys in order, in fp32 with exp2f, from
+// the caches (E4M3 codes decoded and scaled).  Four lanes share a (sequence,
+// query head) row, 32 dimensions each; unit u of rows x heads x 4: lane
+// quarter u % 4, head (u / 4) % H, sequence (u / 4) / H.  Keys in a block
+// outside the pool count as zero vectors (the main pass flags them).
+template <class QT, bool FP8, class SM>
+__device__ __noinline__ void few_key_rows(const AttnParams& p, const SM& sm, int first,
+                                          int stride) {
+  using T = typename QT::T;
+  const int H = p.num_heads;
+  const int lane = threadIdx.x & 31;
+  const unsigned gmask = 0xFu << (lane & 28);
+  const long long units = (long long)p.num_rows * H * 4;
+  for (long long u = first; u < units; u += stride) {
+    const int quarter = (int)(u & 3);
+    const long long ru = u >> 2;
+    const int h = (int)(ru % H);
+    const int s = (int)(ru / H);
+    const int pk = sm.seq_pack[s];
+    if ((sm.seq_pack[s + 1] >> kLenBits) - (pk >> kLenBits) != 1) continue;
+    const int keys = (pk & ((1 << kLenBits) - 1)) + 1;
+    if (keys > kFewKeys) continue;
+    const int kvh = h / p.group;
+    float qf[32];
+    const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
+                                                     ((size_t)s * H + h) * kD + quarter * 32);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) to_float(__ldg(qp + c), qf + 8 * c, QT());
+    float m = -INFINITY, l = 0.0f, acc[32];
+#pragma unroll
+    for (int d = 0; d < 32; ++d) acc[d] = 0.0f;
+    constexpr int kElem = FP8 ? 1 : 2;
+    for (int j = 0; j < keys; ++j) {
+      const int blk = __ldg(p.block_tables + (size_t)s * p.max_blocks_per_seq + j / kBlockSize);
+      const bool bok = blk >= 0 && blk < p.num_blocks;
+      const size_t off = ((((size_t)(bok ? blk : 0) * p.num_kv_heads + kvh) * kBlockSize +
+                           j % kBlockSize) * kD + quarter * 32) * kElem;
+      float kv[32];
+      float dot = 0.0f;
+      if (bok) {
+        const uint4* kp = reinterpret_cast<const uint4*>(p.k_cache + off);
+#pragma unroll
+        for (int c = 0; c < 32 * kElem / 16; ++c) {
+          if constexpr (FP8) to_float(__ldg(kp + c), kv + 16 * c, E4M3());
+          else to_float(__ldg(kp + c), kv + 8 * c, QT());
+        }
+#pragma unroll
+        for (int d = 0; d < 32; ++d) dot = fmaf(qf[d], kv[d], dot);
+      }
+      dot += __shfl_xor_sync(gmask, dot, 1);
+      dot += __shfl_xor_sync(gmask, dot, 2);
+      const float sc = dot * p.q_scale;  // base 2 (with k_scale for E4M3)
+      if (sc > m) {
+        const float a = exp2f(m - sc);
+        l *= a;
+#pragma unroll
+        for (int d = 0; d < 32; ++d) acc[d] *= a;
+        m = sc;
+      }
+      const float w = exp2f(sc - m);
+      l += w;
+      if (bok) {
+        const uint4* vp = reinterpret_cast<const uint4*>(p.v_cache + off);
+#pragma unroll
+        for (int c = 0; c < 32 * kElem / 16; ++c) {
+          if constexpr (FP8) to_float(__ldg(vp + c), kv + 16 * c, E4M3());
+          else to_float(__ldg(vp + c), kv + 8 * c, QT());
+        }
+#pragma unroll
+        for (int d = 0; d < 32; ++d) acc[d] = fmaf(w, kv[d], acc[d]);
+      }
+    }
+    const float inv = p.v_scale / l;
+    T* op = static_cast<T*>(p.out) + ((size_t)s * H + h) * kD + quarter * 32;
+#pragma unroll
+    for (int d = 0; d < 32; ++d) store_out(op + d, acc[d] * inv);
+  }
+}
+
 // Bounded wait that also gives up when another role has aborted.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_test(bar, parity)) return true;
@@ -725,7 +810,10 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
       // one partition and no shared prefix: straight to out
       const bool direct = !split || (x.nparts == 1 && p.prefix_lens == nullptr);
       const size_t head0 = (size_t)x.seq * p.num_heads + (size_t)x.kvh * p.group;
+      // rows with few keys (always direct) are recomputed after the loop
+      const bool few = x.nparts == 1 && p.prefix_lens == nullptr && x.n <= kFewKeys;
       if (direct) {
+        if (few) return true;
         OutT* dst = static_cast<OutT*>(p.out) + head0 * kD + d;
 #pragma unroll
         for (int h = 0; h < L::kRows; ++h)
@@ -889,6 +977,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
     }
     if (ok && have_prev) ok = epilogue(prev, it - 1);
     if (!ok && tid == 0) flag_error(p.errors, PKV_DEVERR_TIMEOUT);
+    if (ok && p.prefix_lens == nullptr) few_key_rows<QT, FP8>(p, sm, cta * 128 + tid, ncta * 128);
   }
 
   tc::fence_before_sync();

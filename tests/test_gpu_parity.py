@@ -130,6 +130,20 @@ def test_decode_block_boundaries(g, kv, D):
     run_case(w)
 
 
+@pytest.mark.parametrize("g", [2, 4, 8, 16])
+@pytest.mark.parametrize("kv", [BF16, E4M3])
+def test_decode_few_keys(g, kv):
+    """Contexts of 2 to 40 tokens, next to long ones: rows that see a few keys,
+    where weights rounded to the MMA input type alone would not meet the
+    tolerance, in launches with and without partition merges."""
+    ctx = list(range(2, 41)) + [1300]
+    w = workloads.independent("few-keys", 1100 + g + kv, ctx, 2 * g, 2, 128, BF16, kv)
+    run_case(w)
+    w = workloads.independent("few-keys-1p", 1200 + g + kv, list(range(2, 41)), 2 * g, 2, 128,
+                              BF16, kv)
+    run_case(w)
+
+
 @pytest.mark.parametrize("ps", [16, 64, 176, 512])
 def test_decode_partition_sizes(ps):
     w = workloads.independent("parts", 2000 + ps, [1, 17, 300, 1024, 1777], 8, 2, 128, F16, F16)
