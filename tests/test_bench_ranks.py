@@ -1,0 +1,43 @@
+"""bench.py's multi-rank host logic on CPU: two gloo ranks (one process each,
+as torchrun would launch them) agree on the slowest rank's time, which the
+whole-job throughput divides by."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        mine = 10.0 + 5.0 * rank  # the second replica is the slow one
+        out[rank] = bench.max_over_ranks(mine, dist, torch.device("cpu"))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_ranks_take_the_slowest_time():
+    world = 2
+    out = mp.Manager().dict()
+    mp.spawn(_rank, args=(world, _free_port(), out), nprocs=world, join=True)
+    assert dict(out) == {0: 15.0, 1: 15.0}
+
+
+def test_single_process_is_unchanged():
+    import bench
+    assert bench.max_over_ranks(3.5) == 3.5
