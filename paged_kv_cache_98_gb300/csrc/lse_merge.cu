@@ -159,17 +159,23 @@ __global__ void __launch_bounds__(32 * kMergeWarps) lse_merge_cta_kernel(const A
     const float4* op =
         reinterpret_cast<const float4*>(p.o_part + head * p.max_parts * D) + lane;
     constexpr int kStride = D / 4;
-    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    constexpr int W = kMergeWarps;
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
     int i = warp;
-    for (; i + kMergeWarps < np; i += 2 * kMergeWarps) {
+    for (; i + 3 * W < np; i += 4 * W) {  // four loads in flight
       const float4 v0 = __ldg(op + (size_t)i * kStride);
-      const float4 v1 = __ldg(op + (size_t)(i + kMergeWarps) * kStride);
+      const float4 v1 = __ldg(op + (size_t)(i + W) * kStride);
+      const float4 v2 = __ldg(op + (size_t)(i + 2 * W) * kStride);
+      const float4 v3 = __ldg(op + (size_t)(i + 3 * W) * kStride);
       a0 = fma4(s_w[i], v0, a0);
-      a1 = fma4(s_w[i + kMergeWarps], v1, a1);
+      a1 = fma4(s_w[i + W], v1, a1);
+      a2 = fma4(s_w[i + 2 * W], v2, a2);
+      a3 = fma4(s_w[i + 3 * W], v3, a3);
     }
-    if (i < np) a0 = fma4(s_w[i], __ldg(op + (size_t)i * kStride), a0);
+    for (; i < np; i += W) a0 = fma4(s_w[i], __ldg(op + (size_t)i * kStride), a0);
     reinterpret_cast<float4*>(s_acc + warp * D)[lane] =
-        make_float4(a0.x + a1.x, a0.y + a1.y, a0.z + a1.z, a0.w + a1.w);
+        make_float4((a0.x + a1.x) + (a2.x + a3.x), (a0.y + a1.y) + (a2.y + a3.y),
+                    (a0.z + a1.z) + (a2.z + a3.z), (a0.w + a1.w) + (a2.w + a3.w));
   }
   __syncthreads();
   if (tid < D) {
