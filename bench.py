@@ -37,6 +37,7 @@ if ROOT not in sys.path:
 
 METRIC = "paged decode KV-read GB/s (% of GB300 HBM peak) and attended tokens/s"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # NVIDIA's GB300 HBM3e figure, context only (not measured here)
 
 
 def parse_args():
@@ -511,6 +512,46 @@ class OracleSample:
         return time.perf_counter() - t0
 
 
+def parallel_oracle_seconds(smp: "OracleSample", threads: int, reps: int = 3) -> float:
+    """The same oracle decode over the sample's sequences split across host
+    threads (the oracle's C calls release the interpreter lock), best of reps."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+    w, o = smp.w, smp.o
+    parts = [p for p in np.array_split(np.arange(w.num_seqs), threads) if len(p)]
+    qsl = np.arange(w.num_seqs)
+
+    def run(ids):
+        o.paged_attention_decode(np.ascontiguousarray(smp.q[qsl[ids]]), smp.kc, smp.vc,
+                                 w.block_tables[ids], w.context_lens[ids], w.num_kv_heads,
+                                 w.head_dim, 16, w.num_blocks, w.scale, 1, smp.kv_dtype, smp.sc,
+                                 smp.sc)
+
+    best = float("inf")
+    with ThreadPoolExecutor(len(parts)) as ex:
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            list(ex.map(run, parts))
+            best = min(best, time.perf_counter() - t0)
+    return best
+
+
+def host_cpu() -> dict:
+    """Host core count and CPU model, for the CPU baselines."""
+    import platform
+    model = platform.processor() or platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"nproc": os.cpu_count(), "cpu": model, "arch": platform.machine()}
+
+
 def oracle_sample(w, budget_s: float) -> OracleSample:
     """The largest sample (KV heads of one sequence, then whole sequences) whose
     step takes about budget_s on one core."""
@@ -606,6 +647,7 @@ def main():
             "parallelism": f"replicas x{world}",
         },
         "attended_tokens_per_s": round(world * tokens / (ms * 1e-3), 1),
+        "sequences_per_s": round(world * w.num_seqs / (ms * 1e-3), 1),
         "hbm_frac": round(world * alg_bytes / (ms * 1e-3) / 1e9 / world / peak, 4),
         "roofline": {
             "kernel": ("cascade decode (shared-prefix pass + own-keys decode + merge launches)"
@@ -614,6 +656,7 @@ def main():
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
             "peak_kind": f"{peak_kind} HBM copy bandwidth",
             "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
             "traffic": recorded_traffic(TRAFFIC_PROFILES.get(
                 args.workload + ("+cascade" if cascade else ""), "")),
             "algorithmic_bytes_per_launch": alg_bytes,
@@ -634,7 +677,14 @@ def main():
         secs = smp.step()
         line["cpu_baseline"] = {"value": round(smp.bytes / secs / 1e9, 4), "unit": "GB/s",
                                 "cores": 1, "kind": "oracle", "sample": smp.desc,
-                                "seconds": round(secs, 2)}
+                                "seconds": round(secs, 2), "host": host_cpu()}
+        # the same oracle functions over the sample's sequences on every host core
+        threads = max(1, min(os.cpu_count() or 1, smp.w.num_seqs))
+        psecs = parallel_oracle_seconds(smp, threads)
+        line["cpu_baseline_parallel"] = {
+            "value": round(smp.bytes / psecs / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle, sequences split over threads", "sample": smp.desc,
+            "seconds": round(psecs, 3)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -665,6 +715,12 @@ def other_workloads(dev, peak, barrier):
             ub = unique_kv_bytes(w)
             d["kv_bytes_unique"] = ub
             d["decode_GBps_unique"] = round(ub / (res["decode_ms"] * 1e-3) / 1e9, 1)
+            # DRAM bytes of one decode launch from the recorded ncu capture (L2 serves
+            # the repeated reads of shared blocks), while the kernel sources match it
+            tr = recorded_traffic(TRAFFIC_PROFILES[name])
+            if tr:
+                d["decode_GBps_dram"] = round(tr / (res["decode_ms"] * 1e-3) / 1e9, 1)
+                d["decode_frac_dram"] = round(tr / (res["decode_ms"] * 1e-3) / 1e9 / peak, 4)
             # the same decode through the cascade entry point (each shared prompt
             # block read once per group of samples)
             cms = st.cascade_timed(steps, 5)
@@ -685,6 +741,8 @@ def other_workloads(dev, peak, barrier):
                 keys = sum(c - ql + i + 1 for i in range(ql))
                 flops += 4 * w.num_heads * w.head_dim * keys
             d["prefill_ms"] = round(res["prefill_ms"], 5)
+            d["prefill_query_tokens_per_s"] = round(
+                float(w.q_lens[w.prefill_ids()].sum()) / (res["prefill_ms"] * 1e-3), 1)
             d["prefill_tflops"] = round(flops / (res["prefill_ms"] * 1e-3) / 1e12, 2)
             d["prefill_flops"] = flops
         if pkv_errors(st):
