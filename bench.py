@@ -544,8 +544,12 @@ def host_cpu() -> dict:
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
-                if line.lower().startswith(("model name", "cpu part")):
+                if line.lower().startswith("model name"):
                     model = line.split(":", 1)[1].strip()
+                    break
+                if line.lower().startswith("cpu part"):  # Arm: the part number
+                    part = line.split(":", 1)[1].strip()
+                    model = {"0xd4f": "Arm Neoverse V2"}.get(part, "Arm") + f" (part {part})"
                     break
     except OSError:
         pass
