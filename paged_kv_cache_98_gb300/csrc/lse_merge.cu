@@ -78,6 +78,15 @@ __global__ void __launch_bounds__(32 * kMergeWarps) lse_merge_warp_kernel(const 
     if (lane < kLanes) store4(out + 4 * lane, make_float4(0.f, 0.f, 0.f, 0.f));
     return;
   }
+  const float4* op = reinterpret_cast<const float4*>(p.o_part + head * p.max_parts * D) +
+                     (lane < kLanes ? lane : 0);
+  constexpr int kStride = D / 4;  // float4s per partial
+  // the first partials are requested before the weights are known
+  constexpr int kPre = 8;
+  float4 pf[kPre];
+#pragma unroll
+  for (int j = 0; j < kPre; ++j)
+    pf[j] = j < np ? __ldg(op + (size_t)j * kStride) : make_float4(0.f, 0.f, 0.f, 0.f);
   // lane j holds the weights of partitions j and j + 32 (np <= kWarpParts = 64)
   const float* lse = p.lse + head * p.max_parts;
   const float l0 = lane < np ? __ldg(lse + lane) : -INFINITY;
@@ -89,13 +98,15 @@ __global__ void __launch_bounds__(32 * kMergeWarps) lse_merge_warp_kernel(const 
   float sum = e0 + e1;
 #pragma unroll
   for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
-  const float4* op = reinterpret_cast<const float4*>(p.o_part + head * p.max_parts * D) +
-                     (lane < kLanes ? lane : 0);
-  constexpr int kStride = D / 4;  // float4s per partial
   float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
   // the whole warp walks the partitions (the weights come by shuffle)
   auto wt = [&](int i) { return __shfl_sync(kFull, i < 32 ? e0 : e1, i & 31); };
-  int i = 0;
+#pragma unroll
+  for (int j = 0; j < kPre; j += 2) {  // weights past np are 0 (their lse is -inf)
+    a0 = fma4(wt(j), pf[j], a0);
+    a1 = fma4(wt(j + 1), pf[j + 1], a1);
+  }
+  int i = kPre;
   for (; i + 4 <= np; i += 4) {
     const float4 v0 = __ldg(op + (size_t)i * kStride), v1 = __ldg(op + (size_t)(i + 1) * kStride);
     const float4 v2 = __ldg(op + (size_t)(i + 2) * kStride), v3 = __ldg(op + (size_t)(i + 3) * kStride);

@@ -303,6 +303,33 @@ def test_full_gqa70b_shared_sampled():
     _full_size(w, sorted(set(g + [longest, 127])))
 
 
+def test_full_gqa70b_cascade_sampled():
+    """The full 70B-GQA workload through the cascade entry point: sampled rows
+    (a whole group, the longest context, the last sequence) against the oracle,
+    and every row against the plain decode's output within twice the tolerance."""
+    w = workloads.gqa70b_shared()
+    g = w.shared_groups[5]
+    longest = int(np.argmax(w.context_lens))
+    sample = sorted(set(g + [longest, 127]))
+    kc, vc, k, v, q, _, _ = _full_size(w, sample)
+    ids, qq, bt, cl = decode_inputs(w, q)
+    gs, pre = w.cascade_groups()
+    mx, mp = int(w.context_lens.max()), int(pre.max())
+    err = errors_word()
+    plain = torch.empty_like(qq)
+    pkv.paged_attention_decode(plain, qq, kc, vc, bt, cl, w.scale, max_context_len=mx)
+    out = torch.empty_like(qq)
+    pkv.paged_attention_decode_cascade(out, qq, kc, vc, bt, cl, torch.from_numpy(gs).cuda(),
+                                       torch.from_numpy(pre).cuda(), w.scale, max_context_len=mx,
+                                       max_prefix_len=mp, device_errors=err)
+    assert pkv.check_errors(err) == 0
+    got = out.float().cpu().numpy()
+    ref = _sampled_oracle(w, k, v, q, [ids[i] for i in sample], 1.0, 1.0)
+    check_close(got[sample], ref, tol(w), "cascade " + w.name)
+    a, r = tol(w)
+    check_close(got, plain.float().cpu().numpy(), (2 * a, 2 * r), "cascade vs plain decode")
+
+
 def test_full_long_fp8_sampled():
     w = workloads.long_fp8()
     _full_size(w, [3], ks_from_data=True)
