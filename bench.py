@@ -375,18 +375,28 @@ class GpuStep:
         self.prefill()
 
     def timed(self, steps: int, warmup: int, barrier=None):
-        """Times `steps` steps; per-step events around the decode and prefill calls."""
+        """Times exactly `steps` steps with one event pair around them (the
+        contract's timed region), then a second pass with events around each
+        call for the per-kernel breakdown."""
         import torch
         for _ in range(warmup):
             self.step()
         torch.cuda.synchronize(self.dev)
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         if barrier:
             barrier()
         torch.cuda.synchronize(self.dev)
         t0.record()
+        for _ in range(steps):
+            self.step()
+        t1.record()
+        torch.cuda.synchronize(self.dev)
+        if barrier:
+            barrier()
+        total = t0.elapsed_time(t1)
+        n = max(1, min(steps, 200))
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
         for e in ev:
             e[0].record()
             self.write()
@@ -395,11 +405,7 @@ class GpuStep:
             e[2].record()
             self.prefill()
             e[3].record()
-        t1.record()
         torch.cuda.synchronize(self.dev)
-        if barrier:
-            barrier()
-        total = t0.elapsed_time(t1)
         dec = [e[1].elapsed_time(e[2]) for e in ev]
         pre = [e[2].elapsed_time(e[3]) for e in ev]
         wr = [e[0].elapsed_time(e[1]) for e in ev]
@@ -408,44 +414,87 @@ class GpuStep:
                 "decode_ms_median": statistics.median(dec)}
 
     def e2e(self, steps: int, warmup: int):
-        """Same step through the public API from pinned host buffers: the step's
-        inputs are copied in and its output read back inside the timed region."""
+        """Same step through the public API from pinned host buffers: every step
+        copies its inputs in and reads its outputs back, inside the timed
+        region.  The copies are pipelined as a server would run them: inputs
+        go to one of two device buffer sets on a copy stream while the
+        previous step computes, and outputs come back on a third stream."""
         import torch
-        host = {}
-        names = ("k_new", "v_new", "slots", "q_dec", "bt", "cl")
+        names = ["k_new", "v_new", "slots", "q_dec", "bt", "cl"]
         if len(self.pre):
-            names += ("q_pre", "bt_pre", "cl_pre", "qsl_pre")
+            names += ["q_pre", "bt_pre", "cl_pre", "qsl_pre"]
         if self.fused:
-            names = ("k_new", "v_new", "slots", "q_all", "bt_all", "cl_all", "qsl_all")
+            names = ["k_new", "v_new", "slots", "q_all", "bt_all", "cl_all", "qsl_all"]
         if self.cascade:
-            names += ("casc_gs", "casc_pre")
-        for name in names:
-            t = getattr(self, name)
-            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-            h.copy_(t)
-            host[name] = h
-        res = self.out_all if self.fused else self.out
-        out_h = torch.empty(res.shape, dtype=res.dtype, pin_memory=True)
-        h2d = sum(h.numel() * h.element_size() for h in host.values())
-        d2h = out_h.numel() * out_h.element_size()
+            names += ["casc_gs", "casc_pre"]
+        outs = ["out_all"] if self.fused else ["out"] + (["out_pre"] if len(self.pre) else [])
+        sets = [{n: getattr(self, n) for n in names + outs},
+                {n: torch.empty_like(getattr(self, n)) for n in names + outs}]
+        host_in = {}
+        for n in names:
+            h = torch.empty(getattr(self, n).shape, dtype=getattr(self, n).dtype, pin_memory=True)
+            h.copy_(getattr(self, n))
+            host_in[n] = h
+        host_out = [{n: torch.empty(sets[0][n].shape, dtype=sets[0][n].dtype, pin_memory=True)
+                     for n in outs} for _ in range(2)]
+        h2d = sum(h.numel() * h.element_size() for h in host_in.values())
+        d2h = sum(h.numel() * h.element_size() for h in host_out[0].values())
+        comp = torch.cuda.current_stream(self.dev)
+        s_in, s_out = torch.cuda.Stream(self.dev), torch.cuda.Stream(self.dev)
+        ev = {k: [torch.cuda.Event(), torch.cuda.Event()] for k in ("in", "comp", "out")}
+        used = [False, False]
 
-        def one():
-            for name, h in host.items():
-                getattr(self, name).copy_(h, non_blocking=True)
+        def run(i):
+            b = i & 1
+            with torch.cuda.stream(s_in):
+                if used[b]:
+                    s_in.wait_event(ev["comp"][b])  # step i - 2 has read set b's inputs
+                for n in names:
+                    sets[b][n].copy_(host_in[n], non_blocking=True)
+                ev["in"][b].record(s_in)
+            comp.wait_event(ev["in"][b])
+            if used[b]:
+                comp.wait_event(ev["out"][b])  # set b's outputs have been read back
+            for n, t in sets[b].items():
+                setattr(self, n, t)
             self.step()
-            out_h.copy_(res, non_blocking=True)
+            ev["comp"][b].record(comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev["comp"][b])
+                for n in outs:
+                    host_out[b][n].copy_(sets[b][n], non_blocking=True)
+                ev["out"][b].record(s_out)
+            used[b] = True
 
-        for _ in range(warmup):
-            one()
+        def drain():
+            for b in range(2):
+                if used[b]:
+                    comp.wait_event(ev["out"][b])
+
+        for i in range(warmup):
+            run(i)
+        drain()
         torch.cuda.synchronize(self.dev)
         a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(steps):
-            one()
-        b.record()
+        z = torch.cuda.Event(enable_timing=True)
+        a.record(comp)
+        s_in.wait_stream(comp)
+        s_out.wait_stream(comp)
+        for i in range(steps):
+            run(warmup + i)
+        drain()
+        z.record(comp)
         torch.cuda.synchronize(self.dev)
-        return a.elapsed_time(b) / steps, h2d, d2h
+        last = host_out[(warmup + steps - 1) & 1]
+        for n, t in sets[0].items():
+            setattr(self, n, t)
+        # the pipelined results are the step's results
+        self.step()
+        torch.cuda.synchronize(self.dev)
+        for n in outs:
+            if not torch.equal(last[n].view(torch.uint8), getattr(self, n).cpu().view(torch.uint8)):
+                raise RuntimeError("pipelined end-to-end step returned a different " + n)
+        return a.elapsed_time(z) / steps, h2d, d2h
 
 
 def unique_kv_bytes(w) -> int:
