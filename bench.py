@@ -725,6 +725,8 @@ def main():
     torch.cuda.empty_cache()
     if not args.no_also and args.workload == "llama2_7b":
         line["also"] = other_workloads(dev, peak, barrier)
+        line["also"]["copy_blocks"] = copy_blocks_rate(dev, peak)
+        line["also"]["host_block_pool"] = host_pool_rate()
     if rank == 0 and not args.no_cpu:
         smp = oracle_sample(w, args.cpu_seconds)
         secs = smp.step()
@@ -743,6 +745,70 @@ def main():
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def copy_blocks_rate(dev, peak, pairs: int = 4096, reps: int = 20) -> dict:
+    """pkv_copy_blocks on a 70B-shaped pool (8 KV heads, head_dim 128, bf16: 32 KB
+    per block and cache): `pairs` random disjoint (source, destination) pairs."""
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_98_gb300 as pkv
+    nb = 4 * pairs
+    kc = torch.zeros((nb, 8, 16, 128), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    perm = np.random.default_rng(11).permutation(nb).astype(np.int32)
+    pr = torch.from_numpy(np.stack([perm[:pairs], perm[pairs:2 * pairs]], 1).copy()).to(dev)
+    for _ in range(3):
+        pkv.copy_blocks(kc, vc, pr)
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    z = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        pkv.copy_blocks(kc, vc, pr)
+    z.record()
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(z) / reps
+    moved = 2 * 2 * pairs * 8 * 16 * 128 * 2  # read + write, K and V
+    return {"pairs": pairs, "ms": round(ms, 5), "GBps": round(moved / (ms * 1e-3) / 1e9, 1),
+            "frac": round(moved / (ms * 1e-3) / 1e9 / peak, 4),
+            "bytes_read_written": moved}
+
+
+def host_pool_rate(requests: int = 20000) -> dict:
+    """The host block pool: requests drawn from 16 shared prompts (200-2000
+    tokens) arrive (prefix match + append of the rest), decode 16 tokens one at
+    a time, and leave; requests per second on one host core."""
+    import numpy as np
+
+    import paged_kv_cache_98_gb300 as pkv
+    r = np.random.default_rng(12)
+    prompts = [r.integers(0, 32000, int(r.integers(200, 2001))).astype(np.int32)
+               for _ in range(16)]
+    pool = pkv.BlockPool(200000)
+    live, hits, toks = [], 0, 0
+    t0 = time.perf_counter()
+    for i in range(requests):
+        p = np.concatenate([prompts[i % 16], r.integers(0, 32000, 20).astype(np.int32)])
+        req = pool.request()
+        m = req.match_prefix(p)
+        hits += m
+        req.append(p[m:])
+        toks += len(p)
+        for j in range(16):
+            req.append(p[j:j + 1])
+        live.append(req)
+        if len(live) > 64:
+            live.pop(0).free()
+    sec = time.perf_counter() - t0
+    for q in live:
+        q.free()
+    pool.close()
+    return {"requests": requests, "seconds": round(sec, 3),
+            "requests_per_s": round(requests / sec, 1),
+            "prefix_hit_frac": round(hits / toks, 4), "cores": 1,
+            "note": "through the Python binding: 18 library calls per request"}
 
 
 def other_workloads(dev, peak, barrier):
