@@ -185,3 +185,24 @@ def test_mixed_workspace_size(lib):
     d = pkv.decode_workspace_size(32, 32, 128, 8192)
     p = pkv.prefill_workspace_size(2048, 32, 128, 8192, 512)
     assert pkv.mixed_workspace_size(32, 2080, 32, 128, 8192) == max(d, p)
+
+
+def test_mixed_workspace_is_checked(lib):
+    # decode rows over 4096 tokens need split-K workspace: missing or short -> PKV_ERR_WORKSPACE
+    f = lib.pkv_paged_attention_mixed
+    args = [256, 256, 512, 512, 1024, 2048, 4096, 2, 4, 40, 16, 8, 2, 128, 16, 256, 4096, 4096,
+            0.1, 1, 1, 1.0, 1.0, 0, None, 0, None, None]
+    assert f(*args) == -3
+    short = list(args)
+    short[24], short[25] = 256, 512
+    assert f(*short) == -3
+
+
+def test_copy_blocks_argument_checks(lib):
+    f = lib.pkv_copy_blocks
+    # caches, pairs, num_pairs, Hkv, D, block_size, num_blocks, dtype, errors, stream
+    assert f(256, 256, 512, 0, 8, 128, 16, 64, 1, None, None) == 0      # nothing to copy
+    assert f(None, 256, 512, 4, 8, 128, 16, 64, 1, None, None) == -1    # no cache
+    assert f(264, 256, 512, 4, 8, 128, 16, 64, 1, None, None) == -1    # misaligned cache
+    assert f(256, 256, 512, 4, 8, 128, 32, 64, 1, None, None) == -2    # block size 32
+    assert f(256, 256, 512, -1, 8, 128, 16, 64, 1, None, None) == -1   # negative count
