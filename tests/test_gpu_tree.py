@@ -98,3 +98,47 @@ def test_unsupported_and_invalid():
     tm = torch.zeros(65, dtype=torch.int64, device="cuda")
     with pytest.raises(pkv.PagedKVError):  # a chunk longer than 64
         pkv.paged_attention_prefill_tree(out, qq, kc, vc, bt, cl, qsl_d, tm, w.scale)
+
+
+def test_full_size_draft_trees_sampled():
+    """A verification batch at serving size: 128 sequences with the 70B-GQA head
+    shape (64 q / 8 kv heads), contexts drawn like that workload's, each with a
+    random 64-token draft tree.  Every output is finite; sampled sequences (the
+    shortest and the longest context, and three more) match the oracle, each
+    computed from a compact cache of its own rows."""
+    r = np.random.default_rng(77)
+    prior = np.clip(np.exp(r.normal(np.log(2000.0), 1.0, size=128)).astype(int), 16, 12000)
+    qlens = [64] * 128
+    w = workloads.independent("tree-full", 78, list(prior + 64), 64, 8, 128, BF16, BF16,
+                              q_lens=qlens)
+    masks = np.concatenate([workloads.tree_mask(workloads.random_tree(r, 64)) for _ in qlens])
+    dev = "cuda"
+    k, v, q = workloads.values_device(w, dev)
+    kc, vc = cache_tensors(w)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    fill_device_cache(w, k, v, kc, vc, errors=err)
+    qq, bt, cl, qsl_d = all_inputs(w, q)
+    out = torch.empty_like(qq)
+    pkv.paged_attention_prefill_tree(out, qq, kc, vc, bt, cl, qsl_d,
+                                     torch.from_numpy(masks.view(np.int64)).cuda(), w.scale,
+                                     max_q_len=64, max_context_len=int(w.context_lens.max()),
+                                     device_errors=err)
+    assert pkv.check_errors(err) == 0
+    got = out.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    qsl = workloads.query_start_loc(w.q_lens)
+    bits = lambda t: t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    for s in sorted({int(np.argmin(prior)), int(np.argmax(prior)), 0, 57, 127}):
+        rows = torch.from_numpy(w.seq_rows[s]).to(dev)
+        c = len(w.seq_rows[s])
+        nb = -(-c // 16)
+        kc_h = np.zeros(nb * 8 * 16 * 128 * 2, np.uint8)
+        vc_h = np.zeros_like(kc_h)
+        oracle.reshape_and_cache(bits(k.index_select(0, rows)), bits(v.index_select(0, rows)),
+                                 kc_h, vc_h, np.arange(c, dtype=np.int64), nb, 16, BF16, BF16)
+        ref = oracle.paged_attention_prefill_tree(
+            bits(q[int(qsl[s]):int(qsl[s + 1])]), kc_h, vc_h,
+            np.arange(nb, dtype=np.int32)[None], np.array([c], np.int32),
+            np.array([0, 64], np.int32), masks[qsl[s]:qsl[s + 1]], 8, 128, 16, nb, w.scale,
+            BF16, BF16)
+        check_close(got[qsl[s]:qsl[s + 1]], ref, tol(w), f"tree sequence {s}")
