@@ -725,6 +725,7 @@ def main():
     torch.cuda.empty_cache()
     if not args.no_also and args.workload == "llama2_7b":
         line["also"] = other_workloads(dev, peak, barrier)
+        line["also"]["tree_verify"] = tree_verify_rate(dev, peak)
         line["also"]["copy_blocks"] = copy_blocks_rate(dev, peak)
         line["also"]["host_block_pool"] = host_pool_rate()
     if rank == 0 and not args.no_cpu:
@@ -745,6 +746,61 @@ def main():
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def tree_verify_rate(dev, peak, reps: int = 50) -> dict:
+    """Draft-tree verification at serving size: 128 sequences with the 70B-GQA head
+    shape (64 q / 8 kv heads), contexts lognormal around 2000 tokens, each with a
+    random 64-token draft tree, in one pkv_paged_attention_prefill_tree call."""
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_98_gb300 as pkv
+    import workloads
+    r = np.random.default_rng(77)
+    prior = np.clip(np.exp(r.normal(np.log(2000.0), 1.0, size=128)).astype(int), 16, 12000)
+    w = workloads.independent("tree-verify", 78, list(prior + 64), 64, 8, 128, workloads.BF16,
+                              workloads.BF16, q_lens=[64] * 128)
+    masks = np.concatenate([workloads.tree_mask(workloads.random_tree(r, 64))
+                            for _ in range(128)])
+    k, v, q = workloads.values_device(w, dev)
+    kc = torch.zeros((w.num_blocks, 8, 16, 128), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    rows = torch.from_numpy(np.concatenate([w.fill_rows, w.new_rows])).to(dev)
+    slots = torch.from_numpy(np.concatenate([w.fill_slots, w.new_slots])).to(dev)
+    pkv.reshape_and_cache(k.index_select(0, rows).contiguous(),
+                          v.index_select(0, rows).contiguous(), kc, vc, slots)
+    bt = torch.from_numpy(np.ascontiguousarray(w.block_tables)).to(dev)
+    cl = torch.from_numpy(np.ascontiguousarray(w.context_lens)).to(dev)
+    qsl = torch.from_numpy(workloads.query_start_loc(w.q_lens)).to(dev)
+    tm = torch.from_numpy(masks.view(np.int64)).to(dev)
+    out = torch.empty_like(q)
+    mx = int(w.context_lens.max())
+
+    def call():
+        pkv.paged_attention_prefill_tree(out, q, kc, vc, bt, cl, qsl, tm, w.scale, max_q_len=64,
+                                         max_context_len=mx)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    z = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        call()
+    z.record()
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(z) / reps
+    kvb = w.kv_read_bytes(np.arange(w.num_seqs))  # every context token once per KV head
+    # visible keys: the prior context for every draft token plus its ancestors in the tree
+    vis = sum(int(w.context_lens[s] - 64) * 64 for s in range(128)) + \
+        sum(bin(int(m)).count("1") for m in masks)
+    flops = 4 * 64 * 128 * vis
+    return {"workload": "128 draft trees of 64 tokens, 64 q / 8 kv heads, bf16, contexts "
+                        f"{int(prior.min())}..{int(prior.max())} + 64",
+            "ms": round(ms, 5), "kv_GBps": round(kvb / (ms * 1e-3) / 1e9, 1),
+            "kv_frac": round(kvb / (ms * 1e-3) / 1e9 / peak, 4),
+            "tflops": round(flops / (ms * 1e-3) / 1e12, 1), "kv_bytes": kvb}
 
 
 def copy_blocks_rate(dev, peak, pairs: int = 4096, reps: int = 20) -> dict:
