@@ -38,11 +38,11 @@
 //
 // Draft-tree mode (speculative verification): a chunk of at most 64 draft
 // tokens whose queries each see the prior context and, of the chunk's own
-// keys, only those in their row of a 64-bit ancestor mask.  A draft token may
-// see only a handful of keys, where rounding its softmax weights to 16 bits no
-// longer averages out; in this mode each weight is also kept as a second
-// 16-bit term (the rounding remainder, in the other 64 columns of S) and P V
-// is accumulated from both, for about 16 significant bits.
+// keys, only those in their row of a 64-bit ancestor mask.  When the prior
+// context is shorter than kFewKeys a draft token may see only a handful of
+// keys, where rounding its softmax weights to 16 bits does not average out:
+// the rows of such chunks are recomputed in fp32 after the main loop, as the
+// causal rows at the start of a prompt are.
 //
 // Warps: 0-3 softmax + epilogue of tile a, 4-7 of tile b, 8 TMEM owner + MMA
 // issuer, 9-11 TMA producers.  A K/V tile is 16 boxes of 16 rows x 128 B (one
@@ -192,12 +192,15 @@ __device__ __forceinline__ bool next_item(const AttnParams& p, const Smem& sm, i
   return true;
 }
 
-// Rows of a causal chunk (qlen queries, the last at position ctx - 1) that
-// see at most kFewKeys keys (positions below kFewKeys); none in draft-tree and
-// shared-prefix modes.
+// Rows of a chunk (qlen queries after ctx - qlen prior tokens) recomputed in
+// fp32: causal rows that see at most kFewKeys keys (positions below
+// kFewKeys); in draft-tree mode every row of a chunk whose prior context is
+// shorter than kFewKeys (a row then sees its prior and its ancestors only);
+// none in shared-prefix mode.
 template <bool kTree, bool kAlt>
 __device__ __forceinline__ int few_rows(int qlen, int ctx) {
-  if (kTree || kAlt) return 0;
+  if (kAlt) return 0;
+  if (kTree) return ctx - qlen < kFewKeys ? qlen : 0;
   const int n = kFewKeys - (ctx - qlen);
   return n <= 0 ? 0 : (n < qlen ? n : qlen);
 }
@@ -266,13 +269,13 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
 
 // kTree: draft-tree mode (per-row ancestor masks over the chunk's keys);
 // kAlt: shared-prefix mode (non-causal, key chunks, partial outputs)
-// The causal rows that see at most kFewKeys keys, recomputed in fp32 from the
-// caches (the plain online softmax over the keys in order, exp2f).  Four
+// The rows that see few keys (few_rows), recomputed in fp32 from the caches
+// (the plain online softmax over the keys in order, exp2f).  Four
 // lanes share a row, 32 dimensions each: partial dot products summed across
 // the four, then each lane's share of the output.  Unit u of F x H x 4 (F
 // such rows): lane quarter u % 4, head (u / 4) % H, row (u / 4) / H.  Keys in
 // a block outside the pool count as zero vectors (the main pass flags them).
-template <class QT>
+template <class QT, bool kTree>
 __device__ __noinline__ void few_key_rows(const AttnParams& p, const Smem& sm, int first,
                                           int stride) {
   using T = typename QT::T;
@@ -291,7 +294,11 @@ __device__ __noinline__ void few_key_rows(const AttnParams& p, const Smem& sm, i
       if (sm.few_start[mid] <= f) lo = mid; else hi = mid - 1;
     }
     const int i = f - sm.few_start[lo];
-    const int pos = sm.seq_ctx[lo] - sm.seq_qlen[lo] + i;  // keys 0 .. pos
+    const int prior = sm.seq_ctx[lo] - sm.seq_qlen[lo];
+    const int pos = prior + i;  // causal: keys 0 .. pos
+    // draft-tree mode: the prior keys, then the chunk keys in the row's mask
+    const uint64_t tmask = kTree ? __ldg(p.tree_mask + sm.seq_q0[lo] + i) : 0ull;
+    const int kend = kTree ? sm.seq_ctx[lo] : pos + 1;
     const int row = sm.seq_q0[lo] + i;
     const int kvh = h / p.group;
     const int trow = p.seq_rows ? __ldg(p.seq_rows + lo) : lo;
@@ -303,7 +310,8 @@ __device__ __noinline__ void few_key_rows(const AttnParams& p, const Smem& sm, i
     float m = -INFINITY, l = 0.0f, acc[32];
 #pragma unroll
     for (int d = 0; d < 32; ++d) acc[d] = 0.0f;
-    for (int j = 0; j <= pos; ++j) {
+    for (int j = 0; j < kend; ++j) {
+      if (kTree && j >= prior && !((tmask >> (j - prior)) & 1ull)) continue;
       const int blk = __ldg(p.block_tables + (size_t)trow * p.max_blocks_per_seq + j / kBlockSize);
       const bool bok = blk >= 0 && blk < p.num_blocks;
       const size_t off = (((size_t)(bok ? blk : 0) * p.num_kv_heads + kvh) * kBlockSize +
@@ -658,14 +666,6 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
           const uint64_t b = kk == ts ? dtail : dv + (uint64_t)((kk * (kBlockSize * 128)) >> 4);
           mma_f16_tmem_a(d, a + kk * 8, b, kIdescO, (t != x.first[qt]) || kk != 0);
         }
-        if (kTree) {  // the weights' rounding remainders
-#pragma unroll
-          for (int kk = 0; kk < kTileKeys / 16; ++kk) {
-            const uint64_t b =
-                kk == ts ? dtail : dv + (uint64_t)((kk * (kBlockSize * 128)) >> 4);
-            mma_f16_tmem_a(d, a + 64 + kk * 8, b, kIdescO, 1u);
-          }
-        }
         if (t == x.last[qt]) tc::mma_commit(&sm.o_done[qt]);
         return true;
       };
@@ -858,42 +858,20 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
 #pragma unroll
           for (int i = 0; i < 8; ++i) l8[i] *= alpha;
         }
-        // P over the first 64 columns of S: keys 2c and 2c+1 in column c; in
-        // draft-tree mode the rounding remainders over the other 64
-        if constexpr (!kTree) {
+        // P over the first 64 columns of S: keys 2c and 2c+1 in column c
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            float pk[16];
+        for (int h = 0; h < 4; ++h) {
+          float pk[16];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int k0 = h * 32 + 2 * c;
-              const float e0 = fast_exp2(fmaf(sv[k0], qa, -m_run));
-              const float e1 = fast_exp2(fmaf(sv[k0 + 1], qa, -m_run));
-              l8[(2 * c) & 7] += e0;
-              l8[(2 * c + 1) & 7] += e1;
-              pk[c] = __uint_as_float(pack2<QT>(e0, e1));
-            }
-            tc::tmem_st16(s_col + 16 * h, pk);
+          for (int c = 0; c < 16; ++c) {
+            const int k0 = h * 32 + 2 * c;
+            const float e0 = fast_exp2(fmaf(sv[k0], qa, -m_run));
+            const float e1 = fast_exp2(fmaf(sv[k0 + 1], qa, -m_run));
+            l8[(2 * c) & 7] += e0;
+            l8[(2 * c + 1) & 7] += e1;
+            pk[c] = __uint_as_float(pack2<QT>(e0, e1));
           }
-        } else {
-#pragma unroll
-          for (int h = 0; h < 8; ++h) {  // 16 keys at a time: weights, then remainders
-            float pk[8], pl[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const int k0 = h * 16 + 2 * c;
-              const float e0 = fast_exp2(fmaf(sv[k0], qa, -m_run));
-              const float e1 = fast_exp2(fmaf(sv[k0 + 1], qa, -m_run));
-              l8[(2 * c) & 7] += e0;
-              l8[(2 * c + 1) & 7] += e1;
-              const uint32_t hi = pack2<QT>(e0, e1);
-              const float2 r = unpack2<QT>(hi);
-              pk[c] = __uint_as_float(hi);
-              pl[c] = __uint_as_float(pack2<QT>(e0 - r.x, e1 - r.y));
-            }
-            tc::tmem_st8(s_col + 8 * h, pk);
-            tc::tmem_st8(s_col + 64 + 8 * h, pl);
-          }
+          tc::tmem_st16(s_col + 16 * h, pk);
         }
         // the product of tile t adds onto O: rescale it first when a row's max moved
         if (t > x.first[qt] && __any_sync(kFull, need)) {
@@ -938,7 +916,8 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
                   make_float4(ov[q4 * 4] * inv, ov[q4 * 4 + 1] * inv, ov[q4 * 4 + 2] * inv,
                               ov[q4 * 4 + 3] * inv);
           }
-        } else if (valid && !(!kTree && !kAlt && qpos < kFewKeys)) {  // few-key rows: later
+        } else if (valid && !(!kAlt && (kTree ? cbase < kFewKeys : qpos < kFewKeys))) {
+          // (rows of few keys are written by few_key_rows after the loop)
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint4 w;
@@ -956,8 +935,8 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
       ++nit;
     }
     if (!ok && tid == 0) flag_error(p.errors, PKV_DEVERR_TIMEOUT);
-    if constexpr (!kTree && !kAlt) {
-      if (ok) few_key_rows<QT>(p, sm, cta * 256 + qt * 128 + tid, ncta * 256);
+    if constexpr (!kAlt) {
+      if (ok) few_key_rows<QT, kTree>(p, sm, cta * 256 + qt * 128 + tid, ncta * 256);
     }
   }
 
