@@ -235,16 +235,6 @@ __device__ __forceinline__ bool all_group(bool ok, int x) {
 }
 
 template <class QT>
-__device__ __forceinline__ float2 unpack2(uint32_t u) {
-  if constexpr (std::is_same<QT, BF16>::value) {
-    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
-  } else {
-    __half2 h = *reinterpret_cast<__half2*>(&u);
-    return __half22float2(h);
-  }
-}
-
-template <class QT>
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
   if constexpr (std::is_same<QT, BF16>::value) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
