@@ -55,6 +55,8 @@ def parse_args():
                          "prompt block once per group, pkv_paged_attention_decode_cascade")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only", choices=["tree_verify", "copy_blocks"],
+                    help="run one of the side measurements alone and print its JSON (profiling)")
     ap.add_argument("--workload", default="llama2_7b",
                     help="named workload of the timed step (default: the LLaMA-2-7B-shaped "
                          "decode); the others are for profiling one workload alone")
@@ -652,6 +654,11 @@ def main():
         if dist:
             dist.barrier()
 
+    if args.only:
+        peak, _ = hbm_peak()
+        fn = tree_verify_rate if args.only == "tree_verify" else copy_blocks_rate
+        print(json.dumps({"only": args.only, **fn(dev, peak)}), flush=True)
+        return
     w = workloads.NAMED[args.workload]()
     cascade = args.decode_entry == "cascade"
     st = GpuStep(w, dev, cascade=cascade, fused=args.mixed_entry == "fused")
