@@ -257,6 +257,29 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
       : "memory");
 }
 
+// The MMAs of one tile, from values passed in registers (nothing in the
+// issue loop is read from memory, so consecutive MMAs issue back to back).
+// Scores: S (128 rows x 128 keys, fp32 in TMEM at d) = Q K^T over head_dim
+// 128, in K-steps of 16 elements within the two 64-element swizzle halves.
+__device__ __forceinline__ void issue_scores(uint32_t d, uint64_t dq, uint64_t dk, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk) {
+    const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+    tc::mma_f16(d, dq + off, dk + off, idesc, kk > 0);
+  }
+}
+
+// Output: O (at d) (+)= P (TMEM at a, 16 keys per 8 columns) V, 16 keys per
+// step; step ts (if >= 0) takes its V rows from the tail buffer.
+__device__ __forceinline__ void issue_pv(uint32_t d, uint32_t a, uint64_t dv, uint64_t dtail, int ts,
+                                         uint32_t acc0, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < kTileKeys / 16; ++kk) {
+    const uint64_t b = kk == ts ? dtail : dv + (uint64_t)((kk * (kBlockSize * 128)) >> 4);
+    mma_f16_tmem_a(d, a + kk * 8, b, idesc, acc0 | (kk != 0 ? 1u : 0u));
+  }
+}
+
 // kTree: draft-tree mode (per-row ancestor masks over the chunk's keys);
 // kAlt: shared-prefix mode (non-causal, key chunks, partial outputs)
 // The rows that see few keys (few_rows), recomputed in fp32 from the caches
@@ -602,7 +625,17 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
     // so each softmax warpgroup works while the tensor pipe serves the other.
     // Shared-prefix mode (warpgroup a even tiles, b odd): S_a(0), S_b(1), then
     //   P_a(t) V_t, S_a(t+2), P_b(t+1) V_t+1, S_b(t+3)   for t = 0, 2, ...
-    if (lane == 0) {
+    // The whole warp runs the loop (waits, counters and descriptors stay warp-
+    // uniform); one elected lane issues the MMAs and commits.
+    {
+      const bool leader = tc::elect_one();
+      auto commit = [&](uint64_t* bar) {
+        if (leader) tc::mma_commit(bar);
+      };
+      // every lane takes the same result
+      auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return __shfl_sync(kFull, (int)wait_bar(bar, parity, abort), 0) != 0;
+      };
       int idx = cta;
       uint32_t pos = 0;
       uint32_t np[2] = {0, 0};   // P tiles consumed per query tile
@@ -616,7 +649,7 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
       constexpr int nst = alt ? kMaxStages : kStages;
       auto acquire = [&](int& st) -> bool {
         st = pos % nst;
-        const bool r = wait_bar(&sm.full[st], (pos / nst) & 1, abort);
+        const bool r = wait(&sm.full[st], (pos / nst) & 1);
         ++pos;
         if (r) tc::fence_after_sync();
         return r;
@@ -631,32 +664,23 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
           tc::smem_desc(smem_u32(&sm.ring[0][0]), kHalf, 1024, tc::kLayoutSw128);
       const uint64_t dtail = tc::smem_desc(taddr, kTailBytes / 2, 1024, tc::kLayoutSw128);
       auto mma_s = [&](int qt, int st) {
-        const uint64_t dk = dk0 + (uint64_t)(st * (kTileBytes >> 4));
-        const uint64_t dqa = dq[qt];
-        const uint32_t d = tmem + qt * 128;
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-          tc::mma_f16(d, dqa + off, dk + off, kIdescS, kk > 0);
-        }
-        tc::mma_commit(&sm.s_ready[qt]);
+        if (leader)
+          issue_scores(tmem + qt * 128, qt ? dq[1] : dq[0],
+                       dk0 + (uint64_t)(st * (kTileBytes >> 4)), kIdescS);
+        commit(&sm.s_ready[qt]);
       };
       auto mma_pv = [&](int qt, int st, int t) -> bool {
-        if (!wait_bar(&sm.p_ready[qt], np[qt] & 1, abort)) return false;
+        if (!wait(&sm.p_ready[qt], np[qt] & 1)) return false;
         ++np[qt];
         if (t == x.first[qt] && nit[qt] >= 1 &&
-            !wait_bar(&sm.o_free[qt], (nit[qt] - 1) & 1, abort))
+            !wait(&sm.o_free[qt], (nit[qt] - 1) & 1))
           return false;  // the previous item's O has been read out
         tc::fence_after_sync();
-        const uint64_t dv = dv0 + (uint64_t)(st * (kTileBytes >> 4));
-        const int ts = t == x.nk - 1 ? x.tail_step : -1;
-        const uint32_t d = tmem + kColO + qt * 128, a = tmem + qt * 128;
-#pragma unroll
-        for (int kk = 0; kk < kTileKeys / 16; ++kk) {
-          const uint64_t b = kk == ts ? dtail : dv + (uint64_t)((kk * (kBlockSize * 128)) >> 4);
-          mma_f16_tmem_a(d, a + kk * 8, b, kIdescO, (t != x.first[qt]) || kk != 0);
-        }
-        if (t == x.last[qt]) tc::mma_commit(&sm.o_done[qt]);
+        if (leader)
+          issue_pv(tmem + kColO + qt * 128, tmem + qt * 128,
+                   dv0 + (uint64_t)(st * (kTileBytes >> 4)), dtail,
+                   t == x.nk - 1 ? x.tail_step : -1, t != x.first[qt], kIdescO);
+        if (t == x.last[qt]) commit(&sm.o_done[qt]);
         return true;
       };
       // K(t) into S of warpgroup qt, its stage released, and Q released after
@@ -665,13 +689,13 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
         int st = 0;
         if (!acquire(st)) return false;
         mma_s(qt, st);
-        tc::mma_commit(&sm.empty[st]);
-        if (t == x.nk - 1) tc::mma_commit(&sm.q_empty);
+        commit(&sm.empty[st]);
+        if (t == x.nk - 1) commit(&sm.q_empty);
         return true;
       };
       auto tail_wait = [&](int t) -> bool {
         if (t != x.nk - 1 || x.tail_step < 0) return true;
-        const bool r = wait_bar(&sm.tail_full, ntail & 1, abort);
+        const bool r = wait(&sm.tail_full, ntail & 1);
         if (r) tc::fence_after_sync();
         return r;
       };
@@ -684,11 +708,11 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
         if (hb && !s_tile(1, x.kt0 + 1)) return false;
         for (int t = x.kt0; t < x.nk; t += 2) {
           if (!(acquire(va) && tail_wait(t) && mma_pv(0, va, t))) return false;
-          tc::mma_commit(&sm.empty[va]);
+          commit(&sm.empty[va]);
           if (t + 2 < x.nk && !s_tile(0, t + 2)) return false;
           if (t + 1 < x.nk) {
             if (!(acquire(vb) && tail_wait(t + 1) && mma_pv(1, vb, t + 1))) return false;
-            tc::mma_commit(&sm.empty[vb]);
+            commit(&sm.empty[vb]);
             if (t + 3 < x.nk && !s_tile(1, t + 3)) return false;
           }
         }
@@ -698,7 +722,7 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
         const bool ha = x.last[0] >= 0;
         const bool hb = x.last[1] >= 0;
         int kst = 0, vst = 0;
-        ok = wait_bar(&sm.q_full, nitem & 1, abort);
+        ok = wait(&sm.q_full, nitem & 1);
         if (ok) tc::fence_after_sync();
         if (ok && x.step == 2) {
           ok = alternate();
@@ -707,8 +731,8 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
           if (ok) {
             if (ha) mma_s(0, kst);
             if (hb) mma_s(1, kst);
-            tc::mma_commit(&sm.empty[kst]);
-            if (x.nk - x.kt0 == 1) tc::mma_commit(&sm.q_empty);
+            commit(&sm.empty[kst]);
+            if (x.nk - x.kt0 == 1) commit(&sm.q_empty);
           }
           for (int t = x.kt0; ok && t < x.nk; ++t) {
             const bool more = t + 1 < x.nk;
@@ -721,24 +745,24 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
             }
             if (ok && hb) ok = mma_pv(1, vst, t);
             if (!ok) break;
-            tc::mma_commit(&sm.empty[vst]);
+            commit(&sm.empty[vst]);
             if (more) {
               if (hb) mma_s(1, kst);
-              tc::mma_commit(&sm.empty[kst]);
-              if (t + 1 == x.nk - 1) tc::mma_commit(&sm.q_empty);
+              commit(&sm.empty[kst]);
+              if (t + 1 == x.nk - 1) commit(&sm.q_empty);
             }
           }
         }
         if (ok && x.tail_step >= 0) {
-          tc::mma_commit(&sm.tail_free);
+          commit(&sm.tail_free);
           ++ntail;
         }
         if (ha) ++nit[0];
         if (hb) ++nit[1];
         ++nitem;
       }
-      if (!ok) flag_error(p.errors, PKV_DEVERR_TIMEOUT);
-      tc::mma_commit(&sm.mma_done);
+      if (!ok && leader) flag_error(p.errors, PKV_DEVERR_TIMEOUT);
+      commit(&sm.mma_done);
       mbar_wait(&sm.mma_done, 0, 100000000ull);
     }
   } else {
