@@ -501,7 +501,17 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
     }
   } else if (warp == 5) {
     // ---- MMA issuer ---------------------------------------------------------------------
-    if (lane == 0) {
+    // The whole warp runs the loop (waits, counters and descriptors stay warp-
+    // uniform); one elected lane issues the MMAs and commits.
+    {
+      const bool leader = tc::elect_one();
+      auto commit = [&](uint64_t* bar) {
+        if (leader) tc::mma_commit(bar);
+      };
+      // every lane takes the same result
+      auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return __shfl_sync(kFull, (int)wait_bar(bar, parity, abort), 0) != 0;
+      };
       int idx = cta;
       uint32_t kpos = 0, vpos = 0;
       int ntail = 0;  // items with a partial last block so far
@@ -510,22 +520,24 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
       bool ok = true;
       auto mma_s = [&](const Item& x, int k) -> bool {
         const int b = k & 1;
-        if (!wait_bar(&sm.q_full[b], (k >> 1) & 1, abort)) return false;
+        if (!wait(&sm.q_full[b], (k >> 1) & 1)) return false;
         const uint32_t qa = smem_u32(&sm.q[b][0]);
         for (int t = 0; t < x.ntiles; ++t, ++kpos) {
           const int st = kpos % KS;
-          if (!wait_bar(&sm.kfull[st], (kpos / KS) & 1, abort)) return false;
+          if (!wait(&sm.kfull[st], (kpos / KS) & 1)) return false;
           tc::fence_after_sync();
           const uint32_t ka = smem_u32(&sm.kring[st][0]);
           const uint32_t d = tmem + b * L::kBufCols + t * L::kSCols;
           if constexpr (FP8) {
             // S^T = K (E4M3, K-major) x [hi; lo]^T, 32 dims per instruction
+            if (leader) {
 #pragma unroll
-            for (int kk = 0; kk < kD / 32; ++kk)
-              tc::mma_f8(d, tc::smem_desc(ka + kk * 32, 16, 1024, tc::kLayoutSw128),
-                         tc::smem_desc(qa + kk * 32, 16, L::kQSbo, tc::kLayoutSw128), kIdescS,
-                         kk > 0);
-          } else {
+              for (int kk = 0; kk < kD / 32; ++kk)
+                tc::mma_f8(d, tc::smem_desc(ka + kk * 32, 16, 1024, tc::kLayoutSw128),
+                           tc::smem_desc(qa + kk * 32, 16, L::kQSbo, tc::kLayoutSw128), kIdescS,
+                           kk > 0);
+            }
+          } else if (leader) {
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk) {
               const uint32_t off = (kk & 3) * 32u;
@@ -537,21 +549,21 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
                           kIdescS, kk > 0);
             }
           }
-          tc::mma_commit(&sm.kempty[st]);
+          commit(&sm.kempty[st]);
         }
-        tc::mma_commit(&sm.s_ready[b]);
-        tc::mma_commit(&sm.q_empty[b]);
+        commit(&sm.s_ready[b]);
+        commit(&sm.q_empty[b]);
         return true;
       };
       auto mma_pv = [&](const Item& x, int k) -> bool {
         const int b = k & 1;
-        if (!wait_bar(&sm.p_ready[b], (k >> 1) & 1, abort)) return false;
+        if (!wait(&sm.p_ready[b], (k >> 1) & 1)) return false;
         // the MMA step that holds the partial block reads the tail buffer
         const bool has_tail = (x.n & (kBlockSize - 1)) != 0;
         const int tail_step = has_tail ? ((x.n - 1) % kTileKeys) / L::kStepKeys : -1;
         const int slot = ntail & 1;
         if (has_tail) {
-          if (!wait_bar(&sm.v_fixed[ntail & 3], (ntail >> 2) & 1, abort)) return false;
+          if (!wait(&sm.v_fixed[ntail & 3], (ntail >> 2) & 1)) return false;
           ++ntail;
         }
         tc::fence_after_sync();
@@ -560,22 +572,24 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
         const uint32_t d = tmem + b * L::kBufCols + L::kOCol;
         for (int t = 0; t < x.ntiles; ++t, ++vpos) {
           const int st = vpos % VS;
-          if (!wait_bar(&sm.vfull[st], (vpos / VS) & 1, abort)) return false;
+          if (!wait(&sm.vfull[st], (vpos / VS) & 1)) return false;
           tc::fence_after_sync();
           const uint32_t va = smem_u32(&sm.vring[st][0]);
           const int ts = t == x.ntiles - 1 ? tail_step : -1;
           if constexpr (FP8) {
             // V^T (E4M3, MN-major: 128 dims = one swizzle atom wide) x
             // P^T (E4M3, K-major), 32 keys per instruction
+            if (leader) {
 #pragma unroll
-            for (int kk = 0; kk < kTileKeys / 32; ++kk) {
-              const uint32_t a = kk == ts ? ta : va + kk * (32 * 128);
-              tc::mma_f8(d, tc::smem_desc(a, 16, 1024, tc::kLayoutSw128),
-                         tc::smem_desc(pa + (t * (kTileKeys / 16) + kk * 2) * 128, 128, L::kPSbo,
-                                       tc::kLayoutNone),
-                         kIdescO, (t | kk) != 0);
+              for (int kk = 0; kk < kTileKeys / 32; ++kk) {
+                const uint32_t a = kk == ts ? ta : va + kk * (32 * 128);
+                tc::mma_f8(d, tc::smem_desc(a, 16, 1024, tc::kLayoutSw128),
+                           tc::smem_desc(pa + (t * (kTileKeys / 16) + kk * 2) * 128, 128,
+                                         L::kPSbo, tc::kLayoutNone),
+                           kIdescO, (t | kk) != 0);
+              }
             }
-          } else {
+          } else if (leader) {
             // V^T (MN-major: two 64-dim atoms) x P^T (K-major), 16 keys per instruction
 #pragma unroll
             for (int kk = 0; kk < kTileKeys / 16; ++kk) {
@@ -589,10 +603,10 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
                           kIdescO, (t | kk) != 0);
             }
           }
-          tc::mma_commit(&sm.vempty[st]);
+          commit(&sm.vempty[st]);
         }
-        if (has_tail) tc::mma_commit(&sm.tail_free[slot]);
-        tc::mma_commit(&sm.o_ready[b]);
+        if (has_tail) commit(&sm.tail_free[slot]);
+        commit(&sm.o_ready[b]);
         return true;
       };
       bool has = next_item(p, sm, idx, total, cur, ncta);
@@ -605,9 +619,9 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
         has = has_n;
         ++it;
       }
-      if (!ok) flag_error(p.errors, PKV_DEVERR_TIMEOUT);
+      if (!ok && leader) flag_error(p.errors, PKV_DEVERR_TIMEOUT);
       // no MMA of ours may still be running when TMEM is released
-      tc::mma_commit(&sm.mma_done);
+      commit(&sm.mma_done);
       mbar_wait(&sm.mma_done, 0, 100000000ull);
     }
   } else if (warp == 7 || (FP8 && warp > 7)) {
