@@ -384,22 +384,44 @@ def copy_blocks(k_cache, v_cache, block_pairs, device_errors=None, stream=None):
     _check("pkv_copy_blocks", rc)
 
 
-def _host_i32(x):
-    import numpy as np
-    a = np.ascontiguousarray(x, dtype=np.int32)
-    return a, a.ctypes.data_as(ctypes.c_void_p)
+class _Scratch:
+    """Host buffers at fixed addresses for the per-token pool calls (token ids
+    in, slots and the copy-on-write pair out), grown on demand: each call then
+    costs one copy in and one copy out instead of fresh ctypes pointers."""
+
+    def __init__(self):
+        import numpy as np
+        self.cap = 0
+        self.cow = np.empty(2, dtype=np.int32)
+        self.cow_addr = self.cow.ctypes.data
+        self.matched = ctypes.c_int32()
+        self.matched_ref = ctypes.byref(self.matched)
+        self.grow(256)
+
+    def grow(self, n: int):
+        import numpy as np
+        if n <= self.cap:
+            return
+        self.cap = max(n, 2 * self.cap)
+        self.tok = np.empty(self.cap, dtype=np.int32)
+        self.slots = np.empty(self.cap, dtype=np.int64)
+        self.tok_addr, self.slots_addr = self.tok.ctypes.data, self.slots.ctypes.data
 
 
 class BlockPool:
     """Host block pool with prefix caching (pkv_block_pool_*): hands out the
-    block tables and slot mappings the attention calls consume."""
+    block tables and slot mappings the attention calls consume. Not thread-safe
+    (one pool per scheduler thread)."""
 
     def __init__(self, num_blocks: int, block_size: int = 16):
         h = ctypes.c_void_p()
+        lib = load()
         _check("pkv_block_pool_create",
-               load().pkv_block_pool_create(num_blocks, block_size, ctypes.byref(h)))
+               lib.pkv_block_pool_create(num_blocks, block_size, ctypes.byref(h)))
         self.h, self.num_blocks, self.block_size = h, num_blocks, block_size
         self._live = set()
+        self._scratch = _Scratch()
+        self._f_append, self._f_match = lib.pkv_request_append, lib.pkv_request_match_prefix
 
     def num_free(self) -> int:
         return load().pkv_block_pool_num_free(self.h)
@@ -458,22 +480,24 @@ class Request:
         pool._live.add(self)
 
     def match_prefix(self, tokens) -> int:
-        a, p = _host_i32(tokens)
-        m = ctypes.c_int32()
+        sc = self.pool._scratch
+        n = len(tokens)
+        sc.grow(n)
+        sc.tok[:n] = tokens
         _check("pkv_request_match_prefix",
-               load().pkv_request_match_prefix(self.h, p, len(a), ctypes.byref(m)))
-        return m.value
+               self.pool._f_match(self.h, sc.tok_addr, n, sc.matched_ref))
+        return sc.matched.value
 
     def append(self, token_ids):
         """Returns (slots int64 numpy array, (source, copy) or None)."""
-        import numpy as np
-        a, p = _host_i32(token_ids)
-        slots = np.empty(max(len(a), 1), dtype=np.int64)
-        cow = np.empty(2, dtype=np.int32)
-        _check("pkv_request_append", load().pkv_request_append(
-            self.h, p, len(a), slots.ctypes.data_as(ctypes.c_void_p),
-            cow.ctypes.data_as(ctypes.c_void_p)))
-        return slots[:len(a)], (None if cow[0] < 0 else (int(cow[0]), int(cow[1])))
+        sc = self.pool._scratch
+        n = len(token_ids)
+        sc.grow(n)
+        sc.tok[:n] = token_ids
+        _check("pkv_request_append",
+               self.pool._f_append(self.h, sc.tok_addr, n, sc.slots_addr, sc.cow_addr))
+        cow = sc.cow
+        return sc.slots[:n].copy(), (None if cow[0] < 0 else (int(cow[0]), int(cow[1])))
 
     def fork(self) -> "Request":
         h = ctypes.c_void_p()
