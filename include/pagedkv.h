@@ -153,8 +153,10 @@ int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
  *
  *   - The array is reserved on every GPU where this entry point is used and
  *     stays reserved until the process exits.
- *   - The first call on a device looks up the array's address (with that
- *     device current); make that first call before any stream capture.
+ *   - The array used is the one on the CURRENT device (cudaGetDevice): make
+ *     the device that holds the tensors current before the call.  The first
+ *     call on a device looks up the array's address (with that device
+ *     current); make that first call before any stream capture.
  *   - Calls whose pkv_decode_workspace_size(...) exceeds
  *     PKV_DECODE_NOALLOC_SCRATCH_BYTES are rejected with PKV_ERR_WORKSPACE
  *     before anything is launched.
@@ -429,6 +431,24 @@ int pkv_requests_block_tables(const pkv_request* const* reqs, int32_t num_reqs,
  * receives the raw bits.
  */
 int pkv_check_errors(uint32_t* device_errors, uint32_t* bits_out, void* stream);
+
+/*
+ * Test hook for the failure detection above (the pages have no counterpart:
+ * "第34讲 …", §1.2 speaks of preemption and service levels only).  Arms the
+ * next attention call made in this process (decode, prefill chunk, draft
+ * tree, mixed batch or cascade): in that call's kernel(s) the first copy
+ * producer of the first CTA does not issue its skip_copy-th tile copy
+ * (counted from 1), and every device-side wait is bounded by wait_limit_us
+ * microseconds (0: the default of about 2 s) instead of the default.  The
+ * waits for the missing tile then run out: the kernel ORs
+ * PKV_DEVERR_TIMEOUT into device_errors, lets its issued copies and MMAs
+ * finish, releases its tensor memory and returns, and pkv_check_errors then
+ * returns PKV_ERR_TIMEOUT.  The rows of that CTA's work are unspecified;
+ * later calls are unaffected.  No copy in flight is ever abandoned and no
+ * GPU fault is raised.  The hook is taken by exactly one call.
+ * PKV_ERR_INVALID_ARG when skip_copy <= 0.
+ */
+int pkv_debug_arm_wait_timeout(int skip_copy, unsigned wait_limit_us);
 
 /* A static, human-readable name for a pkv_status value. */
 const char* pkv_status_string(int status);

@@ -29,6 +29,7 @@ __all__ = [
     "paged_attention_decode_noalloc", "paged_attention_prefill_chunk", "check_errors", "status_string", "version",
     "paged_attention_prefill_tree", "cascade_workspace_size", "paged_attention_decode_cascade",
     "copy_blocks", "BlockPool", "Request", "mixed_workspace_size", "paged_attention_mixed",
+    "debug_arm_wait_timeout",
 ]
 
 F16, BF16, FP8_E4M3 = 0, 1, 2
@@ -94,6 +95,8 @@ def load():
                 [_P] * 8 + [_I] * 10 + [_F, _I, _I, _F, _F, _P, _SZ, _P, _P])
             lib.pkv_check_errors.restype = _I
             lib.pkv_check_errors.argtypes = [_P, _P, _P]
+            lib.pkv_debug_arm_wait_timeout.restype = _I
+            lib.pkv_debug_arm_wait_timeout.argtypes = [_I, ctypes.c_uint]
             lib.pkv_mixed_workspace_size.restype = _SZ
             lib.pkv_mixed_workspace_size.argtypes = [_I] * 5
             lib.pkv_paged_attention_mixed.restype = _I
@@ -305,11 +308,13 @@ def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, conte
     _need_cuda(out, q, k_cache, v_cache, block_tables, context_lens, device_errors)
     S, H, D = q.shape
     nb, hkv, bs, _ = k_cache.shape
-    rc = load().pkv_paged_attention_decode_noalloc(
-        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
-        S, H, hkv, D, bs, block_tables.shape[1], nb, max_context_len, scale, _dtype_code(q),
-        _dtype_code(k_cache), k_scale, v_scale, partition_size, _ptr(device_errors),
-        _stream(stream))
+    # the library takes the scratch array of the current device: make it q's
+    with torch.cuda.device(q.device):
+        rc = load().pkv_paged_attention_decode_noalloc(
+            _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+            _ptr(context_lens), S, H, hkv, D, bs, block_tables.shape[1], nb, max_context_len,
+            scale, _dtype_code(q), _dtype_code(k_cache), k_scale, v_scale, partition_size,
+            _ptr(device_errors), _stream(stream))
     _check("pkv_paged_attention_decode_noalloc", rc)
     return out
 
@@ -520,6 +525,14 @@ class Request:
             load().pkv_request_free(self.h)
             self.h = None
             self.pool._live.discard(self)
+
+
+def debug_arm_wait_timeout(skip_copy: int, wait_limit_us: int = 0) -> None:
+    """Test hook: the next attention call's first CTA skips its skip_copy-th
+    tile copy and its device waits give up after wait_limit_us, so the call
+    reports a wait timeout through its error word (pkv_debug_arm_wait_timeout)."""
+    _check("pkv_debug_arm_wait_timeout", load().pkv_debug_arm_wait_timeout(skip_copy,
+                                                                            wait_limit_us))
 
 
 def check_errors(device_errors, stream=None) -> int:

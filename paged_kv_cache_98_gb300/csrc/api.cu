@@ -1,6 +1,7 @@
 // C ABI of libpagedkv.so: argument validation and kernel dispatch.  The
 // declarations, data model and error conventions are in include/pagedkv.h.
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -89,6 +90,7 @@ int run_attention(pkv::AttnParams& p, int q_dtype, int kv_dtype, int head_dim, f
   p.q_scale = scale * pkv::kLog2e * (fp8 ? k_scale : 1.0f);
   p.v_scale = fp8 ? v_scale : 1.0f;
   const int g_pad = pow2_at_least(p.group);
+  pkv::take_debug_hook(p);
   int rc;
   if (pkv::tc_decode_supported(p, q_dtype, kv_dtype, head_dim))
     rc = pkv::launch_paged_decode_tc(p, q_dtype, kv_dtype, stream);
@@ -102,6 +104,18 @@ int run_attention(pkv::AttnParams& p, int q_dtype, int kv_dtype, int head_dim, f
 }  // namespace
 
 namespace pkv {
+
+// The failure-detection test hook armed by pkv_debug_arm_wait_timeout: taken
+// (and cleared) by the next attention call.
+std::atomic<int> g_hook_skip{0};
+std::atomic<unsigned long long> g_hook_limit_ns{0};
+
+void take_debug_hook(AttnParams& p) {
+  if (g_hook_skip.load(std::memory_order_relaxed) == 0) return;
+  p.skip_copy = g_hook_skip.exchange(0);
+  p.wait_limit_ns = g_hook_limit_ns.exchange(0);
+}
+
 int launch_paged_attention_simt(const AttnParams& p, int q_dtype, int kv_dtype, int head_dim,
                                 int g_pad, cudaStream_t stream) {
   if (q_dtype == PKV_F16)
@@ -253,6 +267,7 @@ int pkv_paged_attention_prefill_chunk(void* out, const void* q, const void* k_ca
     const bool fp8 = kv_dtype == PKV_FP8_E4M3;
     p.q_scale = scale * pkv::kLog2e * (fp8 ? k_scale : 1.0f);
     p.v_scale = fp8 ? v_scale : 1.0f;
+    pkv::take_debug_hook(p);
     return pkv::launch_prefill_tc(p, q_dtype, total_q, static_cast<cudaStream_t>(stream));
   }
   const size_t need = split_workspace((size_t)total_q, num_heads, head_dim, p.max_parts);
@@ -301,6 +316,7 @@ int pkv_paged_attention_prefill_tree(void* out, const void* q, const void* k_cac
   if (!pkv::tc_prefill_supported(p, q_dtype, kv_dtype, head_dim)) return PKV_ERR_UNSUPPORTED;
   p.q_scale = scale * pkv::kLog2e;
   p.v_scale = 1.0f;
+  pkv::take_debug_hook(p);
   return pkv::launch_prefill_tc(p, q_dtype, total_q, static_cast<cudaStream_t>(stream));
 }
 
@@ -393,6 +409,9 @@ int pkv_paged_attention_mixed(void* out, const void* q, const void* k_cache, con
   }
   pd.q_scale = pp.q_scale = scale * pkv::kLog2e;
   pd.v_scale = pp.v_scale = 1.0f;
+  pkv::take_debug_hook(pd);
+  pp.skip_copy = pd.skip_copy;
+  pp.wait_limit_ns = pd.wait_limit_ns;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   rc = pkv::launch_mixed_tc(pd, pp, q_dtype, total_q, prefill_ctas, st);
   if (rc != PKV_OK) return rc;
@@ -456,6 +475,7 @@ int pkv_paged_attention_decode_cascade(void* out, const void* q, const void* k_c
   p.q_scale = scale * pkv::kLog2e;
   p.v_scale = 1.0f;
   p.prefix_chunk = kCascadeChunk;
+  pkv::take_debug_hook(p);
   // pass 1: every member's query over its group's shared prefix (the prefill
   // kernel, no causal mask, one partial per chunk of the prefix)
   pkv::AttnParams pp = p;
@@ -488,6 +508,13 @@ int pkv_paged_attention_decode_cascade(void* out, const void* q, const void* k_c
   rc = pkv::launch_paged_decode_tc(ps, q_dtype, kv_dtype, st);
   if (rc != PKV_OK) return rc;
   return pkv::launch_lse_merge(ps, q_dtype, head_dim, st);
+}
+
+int pkv_debug_arm_wait_timeout(int skip_copy, unsigned wait_limit_us) {
+  if (skip_copy <= 0) return PKV_ERR_INVALID_ARG;
+  pkv::g_hook_limit_ns.store((unsigned long long)wait_limit_us * 1000ull);
+  pkv::g_hook_skip.store(skip_copy);
+  return PKV_OK;
 }
 
 int pkv_check_errors(uint32_t* device_errors, uint32_t* bits_out, void* stream) {

@@ -275,15 +275,16 @@ __device__ __noinline__ void few_key_rows(const AttnParams& p, const SM& sm, int
   }
 }
 
-// Bounded wait that also gives up when another role has aborted.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// Wait bounded by limit_ns that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                         unsigned long long limit_ns) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_test(bar, parity)) return true;
     if ((it & 63u) == 63u) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > 2000000000ull) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort = 1;
         return false;
       }
@@ -413,6 +414,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
   tc::fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort = &sm.abort;
+  const unsigned long long lim = wait_limit(p);
   const int total = (sm.seq_pack[p.num_rows] >> kLenBits) * p.num_kv_heads;
 
   if (warp == 4 || warp == 6 || warp == kWarpK1 || warp == kWarpV1) {
@@ -451,7 +453,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
       const int b = k & 1;
       bool good = true;
       if (lane == 0) {
-        if (k >= 2) good = wait_bar(&sm.q_empty[b], ((k - 2) >> 1) & 1, abort);
+        if (k >= 2) good = wait_bar(&sm.q_empty[b], ((k - 2) >> 1) & 1, abort, lim);
         if (good) {
           mbar_arrive_expect_tx(&sm.q_full[b], L::kQBytes);
           const int row = x.seq * p.num_heads + x.kvh * p.group;
@@ -464,13 +466,16 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
     auto load_tiles = [&](const Item& x, int row) -> bool {
       for (int t = 0; t < x.ntiles; ++t, ++pos) {
         const uint32_t st = pos % nst;
+        // test hook: this copy is never issued, so every wait for the tile runs out
+        const bool skip = !is_v && pi == 0 && cta == 0 && p.skip_copy > 0 &&
+                          pos + 1 == (uint32_t)p.skip_copy;
         bool good = true;
         if (lane == 0) {
-          if (pos >= nst) good = wait_bar(&empty[st], ((pos / nst) - 1) & 1, abort);
-          if (good) mbar_arrive_expect_tx(&full[st], L::kTileBytes / kProd);
+          if (pos >= nst) good = wait_bar(&empty[st], ((pos / nst) - 1) & 1, abort, lim);
+          if (good && !skip) mbar_arrive_expect_tx(&full[st], L::kTileBytes / kProd);
         }
         if (!__shfl_sync(kFull, (int)good, 0)) return false;
-        if ((lane >> 3) == t && my_block) {
+        if (!skip && (lane >> 3) == t && my_block) {
           uint8_t* dst = ring + (size_t)st * L::kTileBytes + (lane & 7) * (kBlockSize * 128);
           tc::tma_load_2d(dst, map, 0, row, &full[st]);
           if (!FP8) tc::tma_load_2d(dst + kHalfBytes, map, 64, row, &full[st]);
@@ -510,7 +515,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
       };
       // every lane takes the same result
       auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-        return __shfl_sync(kFull, (int)wait_bar(bar, parity, abort), 0) != 0;
+        return __shfl_sync(kFull, (int)wait_bar(bar, parity, abort, lim), 0) != 0;
       };
       int idx = cta;
       uint32_t kpos = 0, vpos = 0;
@@ -670,7 +675,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
       }
       const int m = ntail;
       bool good = true;
-      if (m >= 2) good = wait_bar(&sm.tail_free[m & 1], ((m - 2) >> 1) & 1, abort);
+      if (m >= 2) good = wait_bar(&sm.tail_free[m & 1], ((m - 2) >> 1) & 1, abort, lim);
       if (!group_all(good)) return false;
       uint8_t* slot = &sm.tail[m & 1][0];
 #pragma unroll
@@ -710,7 +715,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
       auto conv_q = [&](const uint4* buf, int k) -> bool {
         const int b = k & 1;
         bool good = true;
-        if (k >= 2) good = wait_bar(&sm.q_empty[b], ((k - 2) >> 1) & 1, abort);
+        if (k >= 2) good = wait_bar(&sm.q_empty[b], ((k - 2) >> 1) & 1, abort, lim);
         if (!all_of_group<2>(good)) return false;
         float f[EPT];
 #pragma unroll
@@ -813,7 +818,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
 
     auto epilogue = [&](const Item& x, int k) -> bool {
       const int b = k & 1;
-      const bool ok = all_softmax(wait_bar(&sm.o_ready[b], (k >> 1) & 1, abort));
+      const bool ok = all_softmax(wait_bar(&sm.o_ready[b], (k >> 1) & 1, abort, lim));
       if (!ok) return false;
       tc::fence_after_sync();
       float o[16];
@@ -848,13 +853,13 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
     while (has) {
       const bool has_n = next_item(p, sm, idx, total, nxt, ncta);
       const int b = it & 1;
-      ok = all_softmax(wait_bar(&sm.s_ready[b], (it >> 1) & 1, abort));
+      ok = all_softmax(wait_bar(&sm.s_ready[b], (it >> 1) & 1, abort, lim));
       if (!ok) break;
       tc::fence_after_sync();
       float qsh[16];  // scale of each head's scores (base 2)
       if constexpr (FP8) {
         // per-row scales of the split query: published by the converters
-        ok = all_softmax(wait_bar(&sm.qs_ready[it & 3], (it >> 2) & 1, abort));
+        ok = all_softmax(wait_bar(&sm.qs_ready[it & 3], (it >> 2) & 1, abort, lim));
         if (!ok) break;
 #pragma unroll
         for (int h = 0; h < L::kRows; ++h) qsh[h] = qs * sm.qscale[it & 3][h];

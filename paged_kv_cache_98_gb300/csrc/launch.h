@@ -8,6 +8,10 @@
 
 namespace pkv {
 
+// Longest a device-side wait may take before the kernel gives up, flags
+// PKV_DEVERR_TIMEOUT and returns (about 2 s).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
 // One launch of the paged attention kernels.  A "row" is one query token:
 // a decode sequence (query_start_loc == nullptr, row = sequence) or one query
 // of a prefill chunk (row = index into q, its sequence found through
@@ -47,7 +51,21 @@ struct AttnParams {
   // Draft-tree verification (prefill): per query row, bit j = the chunk's key
   // j is visible (its ancestors and itself); null = causal.
   const uint64_t* tree_mask;
+  // Failure-detection test hook (zero in normal calls): the longest any
+  // device-side wait of the launch may take (0: kWaitLimitNs), and a copy
+  // the first producer of CTA 0 never issues (n > 0: its n-th tile copy,
+  // counted from 1), so that the waits for that tile run out.
+  unsigned long long wait_limit_ns;
+  int skip_copy;
 };
+
+// Limit of the launch's device-side waits.
+__host__ __device__ inline unsigned long long wait_limit(const AttnParams& p) {
+  return p.wait_limit_ns ? p.wait_limit_ns : kWaitLimitNs;
+}
+
+// Applies and clears the armed test hook (pkv_debug_arm_wait_timeout), if any.
+void take_debug_hook(AttnParams& p);
 
 int launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, int num_tokens, int num_kv_heads,

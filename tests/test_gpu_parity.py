@@ -6,6 +6,9 @@ within |gpu - ref| <= 2e-3 + 1e-2 |ref| (fp16/bf16 caches) or
 the CUDA path produced: it builds its own cache from the same seeded source
 rows with its own cache write.
 """
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 import torch
@@ -239,35 +242,53 @@ def test_device_checks_flag_bad_inputs():
     assert pkv.check_errors(err) == 0
 
 
-# ---- full-size workloads, sampled sequences -----------------------------------------
+# ---- full-size workloads: every sequence against the oracle ------------------------------
+def _workers(n):
+    return max(1, min(n, os.cpu_count() or 1))
+
+
+def _seq_bits(t, rows):
+    """Source rows of one sequence as host uint16 bits."""
+    return t.index_select(0, rows).cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _compact(w, c):
+    """A one-sequence workload of c tokens on consecutive blocks 0.. (the
+    oracle's result does not depend on the physical layout)."""
+    nb = -(-c // 16)
+    return workloads.Workload(
+        name="sample", num_heads=w.num_heads, num_kv_heads=w.num_kv_heads,
+        head_dim=w.head_dim, q_dtype=w.q_dtype, kv_dtype=w.kv_dtype, num_blocks=nb,
+        context_lens=np.array([c], np.int32), q_lens=np.array([1], np.int32),
+        block_tables=np.arange(nb, dtype=np.int32)[None], seq_rows=[np.arange(c)],
+        num_src_rows=c, fill_rows=np.arange(c, dtype=np.int64),
+        fill_slots=np.arange(c, dtype=np.int64), new_rows=np.zeros(0, np.int64),
+        new_slots=np.zeros(0, np.int64), scale=w.scale, src_dtype=w.src_dtype)
+
+
 def _sampled_oracle(w, k_src, v_src, q_all, sample, ks=1.0, vs=1.0):
-    """Oracle output of the sampled decode sequences, each from a compact cache of
-    its own source rows (the result does not depend on the physical layout)."""
+    """Oracle output of the given decode sequences, each from a compact cache of
+    its own source rows, one sequence per host thread (the oracle's C calls
+    release the interpreter lock)."""
     qsl = workloads.query_start_loc(w.q_lens)
-    outs = []
-    for s in sample:
+
+    def one(s):
         rows = torch.from_numpy(w.seq_rows[s]).to(k_src.device)
-        kb = k_src.index_select(0, rows).cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-        vb = v_src.index_select(0, rows).cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-        c = len(w.seq_rows[s])
-        nb = -(-c // 16)
-        sub = workloads.Workload(
-            name="sample", num_heads=w.num_heads, num_kv_heads=w.num_kv_heads,
-            head_dim=w.head_dim, q_dtype=w.q_dtype, kv_dtype=w.kv_dtype, num_blocks=nb,
-            context_lens=np.array([c], np.int32), q_lens=np.array([1], np.int32),
-            block_tables=np.arange(nb, dtype=np.int32)[None], seq_rows=[np.arange(c)],
-            num_src_rows=c, fill_rows=np.arange(c, dtype=np.int64),
-            fill_slots=np.arange(c, dtype=np.int64), new_rows=np.zeros(0, np.int64),
-            new_slots=np.zeros(0, np.int64), scale=w.scale, src_dtype=w.src_dtype)
+        kb, vb = _seq_bits(k_src, rows), _seq_bits(v_src, rows)
+        sub = _compact(w, len(w.seq_rows[s]))
         kc_h, vc_h = host_cache(sub, kb, vb, ks, vs)
         qh = q_all[int(qsl[s]):int(qsl[s]) + 1].cpu().contiguous().view(torch.int16).numpy()
-        outs.append(oracle.paged_attention_decode(
+        return oracle.paged_attention_decode(
             qh.view(np.uint16), kc_h, vc_h, sub.block_tables, sub.context_lens, w.num_kv_heads,
-            w.head_dim, 16, nb, w.scale, w.q_dtype, w.kv_dtype, ks, vs)[0])
-    return np.stack(outs)
+            w.head_dim, 16, sub.num_blocks, w.scale, w.q_dtype, w.kv_dtype, ks, vs)[0]
+
+    with ThreadPoolExecutor(_workers(len(sample))) as ex:
+        return np.stack(list(ex.map(one, sample)))
 
 
-def _full_size(w, sample, ks_from_data=False):
+def _full_size(w, ks_from_data=False):
+    """Runs the workload's decode at full size and compares EVERY sequence with
+    the oracle; returns the device state and the oracle's output."""
     dev = "cuda"
     k, v, q = workloads.values_device(w, dev)
     ks = vs = 1.0
@@ -284,58 +305,41 @@ def _full_size(w, sample, ks_from_data=False):
                                v_scale=vs, device_errors=err)
     assert pkv.check_errors(err) == 0
     got = out.float().cpu().numpy()
-    ref = _sampled_oracle(w, k, v, q, [ids[i] for i in sample], ks, vs)
-    check_close(got[sample], ref, tol(w), w.name)
-    assert np.all(np.isfinite(got))
-    return kc, vc, k, v, q, ks, vs
+    ref = _sampled_oracle(w, k, v, q, list(ids), ks, vs)
+    check_close(got, ref, tol(w), w.name)
+    return kc, vc, k, v, q, ks, vs, ref
 
 
-def test_full_llama2_7b_sampled():
-    w = workloads.llama2_7b()
-    _full_size(w, [0, 31, 63])
+def test_full_llama2_7b_every_sequence():
+    _full_size(workloads.llama2_7b())
 
 
-def test_full_gqa70b_shared_sampled():
+def test_full_gqa70b_shared_and_cascade_every_sequence():
+    """The full 70B-GQA workload, every sequence, through plain decode and
+    through the cascade entry point (shared prompts read once per group)."""
     w = workloads.gqa70b_shared()
-    g = w.shared_groups[5]
-    lens = w.context_lens
-    longest = int(np.argmax(lens))
-    _full_size(w, sorted(set(g + [longest, 127])))
-
-
-def test_full_gqa70b_cascade_sampled():
-    """The full 70B-GQA workload through the cascade entry point: sampled rows
-    (a whole group, the longest context, the last sequence) against the oracle,
-    and every row against the plain decode's output within twice the tolerance."""
-    w = workloads.gqa70b_shared()
-    g = w.shared_groups[5]
-    longest = int(np.argmax(w.context_lens))
-    sample = sorted(set(g + [longest, 127]))
-    kc, vc, k, v, q, _, _ = _full_size(w, sample)
+    kc, vc, k, v, q, _, _, ref = _full_size(w)
     ids, qq, bt, cl = decode_inputs(w, q)
     gs, pre = w.cascade_groups()
     mx, mp = int(w.context_lens.max()), int(pre.max())
     err = errors_word()
-    plain = torch.empty_like(qq)
-    pkv.paged_attention_decode(plain, qq, kc, vc, bt, cl, w.scale, max_context_len=mx)
     out = torch.empty_like(qq)
     pkv.paged_attention_decode_cascade(out, qq, kc, vc, bt, cl, torch.from_numpy(gs).cuda(),
                                        torch.from_numpy(pre).cuda(), w.scale, max_context_len=mx,
                                        max_prefix_len=mp, device_errors=err)
     assert pkv.check_errors(err) == 0
-    got = out.float().cpu().numpy()
-    ref = _sampled_oracle(w, k, v, q, [ids[i] for i in sample], 1.0, 1.0)
-    check_close(got[sample], ref, tol(w), "cascade " + w.name)
-    a, r = tol(w)
-    check_close(got, plain.float().cpu().numpy(), (2 * a, 2 * r), "cascade vs plain decode")
+    check_close(out.float().cpu().numpy(), ref, tol(w), "cascade " + w.name)
 
 
-def test_full_long_fp8_sampled():
-    w = workloads.long_fp8()
-    _full_size(w, [3], ks_from_data=True)
+def test_full_long_fp8_every_sequence():
+    _full_size(workloads.long_fp8(), ks_from_data=True)
 
 
-def test_full_mixed_sampled():
+def test_full_mixed_every_row():
+    """Mixed batch at full size: all 32 decode rows and all 4 chunks of 512
+    queries against the oracle.  Each chunk is checked in slices of 64
+    queries: a slice of a chunk is itself a chunk (same block table, context
+    cut after its last query), so the slices run on separate host threads."""
     w = workloads.mixed()
     dev = "cuda"
     k, v, q = workloads.values_device(w, dev)
@@ -346,31 +350,62 @@ def test_full_mixed_sampled():
     out = torch.empty_like(qq)
     pkv.paged_attention_decode(out, qq, kc, vc, bt, cl, w.scale,
                                max_context_len=int(w.context_lens[ids].max()), device_errors=err)
-    sample = [0, 17, 31]
-    ref = _sampled_oracle(w, k, v, q, [ids[i] for i in sample])
-    check_close(out.float().cpu().numpy()[sample], ref, tol(w), "mixed decode")
     pids, pq, pbt, pcl, pqsl = prefill_inputs(w, q)
     pout = torch.empty_like(pq)
     pkv.paged_attention_prefill_chunk(pout, pq, kc, vc, pbt, pcl, pqsl, w.scale,
                                       max_q_len=512, max_context_len=2560, device_errors=err)
     assert pkv.check_errors(err) == 0
-    # one prefill sequence in full through the oracle
-    s = pids[1]
-    rows = torch.from_numpy(w.seq_rows[s]).to(dev)
-    kb = k.index_select(0, rows).cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-    vb = v.index_select(0, rows).cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-    c = len(w.seq_rows[s])
-    nb = -(-c // 16)
-    kc_h = np.zeros(nb * w.num_kv_heads * 16 * w.head_dim * 2, np.uint8)
-    vc_h = np.zeros_like(kc_h)
-    oracle.reshape_and_cache(kb, vb, kc_h, vc_h, np.arange(c), nb, 16, BF16, BF16)
+    ref = _sampled_oracle(w, k, v, q, list(ids))
+    check_close(out.float().cpu().numpy(), ref, tol(w), "mixed decode rows")
     qsl = workloads.query_start_loc(w.q_lens)
-    qh = q[int(qsl[s]):int(qsl[s + 1])].cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-    ref = oracle.paged_attention_prefill(qh, kc_h, vc_h, np.arange(nb, dtype=np.int32)[None],
-                                         np.array([c], np.int32), np.array([0, 512], np.int32),
-                                         w.num_kv_heads, w.head_dim, 16, nb, w.scale, BF16, BF16)
-    got = pout[512:1024].float().cpu().numpy()
-    check_close(got, ref, tol(w), "mixed prefill")
+    caches = {}
+    for s in pids:
+        rows = torch.from_numpy(w.seq_rows[s]).to(dev)
+        sub = _compact(w, len(w.seq_rows[s]))
+        caches[s] = (sub, host_cache(sub, _seq_bits(k, rows), _seq_bits(v, rows)))
+    qh_all = q.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    step = 64
+
+    def one(task):
+        s, a = task
+        sub, (kc_h, vc_h) = caches[s]
+        c = int(sub.context_lens[0])
+        qlen = int(w.q_lens[s])
+        b = min(a + step, qlen)
+        qh = np.ascontiguousarray(qh_all[int(qsl[s]) + a:int(qsl[s]) + b])
+        return oracle.paged_attention_prefill(
+            qh, kc_h, vc_h, sub.block_tables, np.array([c - qlen + b], np.int32),
+            np.array([0, b - a], np.int32), w.num_kv_heads, w.head_dim, 16, sub.num_blocks,
+            w.scale, BF16, BF16)
+
+    tasks = [(s, a) for s in pids for a in range(0, int(w.q_lens[s]), step)]
+    with ThreadPoolExecutor(_workers(len(tasks))) as ex:
+        parts = list(ex.map(one, tasks))
+    got = pout.float().cpu().numpy()
+    base = {s: sum(int(w.q_lens[t]) for t in pids if t < s) for s in pids}
+    for (s, a), r in zip(tasks, parts):
+        check_close(got[base[s] + a:base[s] + a + len(r)], r, tol(w), f"mixed chunk {s} @{a}")
+
+
+def test_full_mixed_cache_write_bit_exact():
+    """The mixed step's cache write at full size (2,080 new tokens through its
+    random slot mapping into the 8-head pool), compared byte for byte with the
+    oracle's cache write over the whole K and V caches."""
+    w = workloads.mixed()
+    k, v, _ = workloads.values_device(w, "cuda")
+    kc, vc = cache_tensors(w, sentinel=0x5A)
+    err = errors_word()
+    r = torch.from_numpy(w.new_rows).cuda()
+    kn, vn = k.index_select(0, r).contiguous(), v.index_select(0, r).contiguous()
+    assert kn.shape[0] == 2080
+    pkv.reshape_and_cache(kn, vn, kc, vc, torch.from_numpy(w.new_slots).cuda(), device_errors=err)
+    assert pkv.check_errors(err) == 0
+    kc_h = np.full(cache_bytes(w), 0x5A, np.uint8)
+    vc_h = np.full(cache_bytes(w), 0x5A, np.uint8)
+    oracle.reshape_and_cache(_seq_bits(k, r), _seq_bits(v, r), kc_h, vc_h, w.new_slots,
+                             w.num_blocks, 16, BF16, BF16)
+    assert np.array_equal(kc.view(torch.uint8).cpu().numpy().reshape(-1), kc_h)
+    assert np.array_equal(vc.view(torch.uint8).cpu().numpy().reshape(-1), vc_h)
 
 
 def test_decode_many_sequences_chunked_launches():

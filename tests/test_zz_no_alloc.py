@@ -1,8 +1,12 @@
 """The allocation-free decode entry point, for callers that may not allocate
 device memory (a host framework owning every byte through its own pool, or a
 loop that must not pay cudaMalloc/cudaFree synchronisation).  It must give the
-same output as the workspace entry point, call after call, although every call
-reuses the library's one fixed scratch array.
+same output as the workspace entry point and as the CPU oracle, call after
+call, although every call reuses the library's one fixed scratch array.
+
+The second call of each pair reads fewer partitions, of other sequences, than
+the first wrote, so a read of the previous call's partials or log-sum-exps
+from the shared array would show up as a mismatch.
 
 This file sorts last so that a run stopping at the first failure has already
 run every other test; it also passes on its own in a fresh process.
@@ -13,10 +17,11 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_98_gb300 as pkv
 import workloads
-from _gpu import TOL_16BIT, TOL_FP8, bits_to_dev, cache_tensors, check_close, decode_inputs, \
-    fill_device_cache
+from _gpu import TOL_16BIT, TOL_FP8, bits_to_dev, cache_tensors, check_close, fill_device_cache
+from _util import host_cache
 
 pytestmark = pytest.mark.gpu
 
@@ -28,27 +33,36 @@ def _library():
     pkv.load()
 
 
-def _setup(w):
+@pytest.mark.parametrize("kv", [workloads.BF16, workloads.E4M3])
+def test_noalloc_matches_workspace_entry_and_oracle_two_calls_in_a_row(kv):
+    # contexts long enough for several 512-token partitions, so the scratch is used
+    ctx = [3000, 1, 700, 2600, 1536, 17]
+    w = workloads.independent("noalloc", 61 + kv, ctx, 16, 4, 128, workloads.BF16, kv)
     k, v, q = workloads.values_cpu(w)
     # E4M3 caches: a fixed per-tensor scale (N(0,1) values stay below 448 * scale)
-    ks = vs = 0.02 if w.kv_dtype == workloads.E4M3 else 1.0
+    ks = vs = 0.02 if kv == workloads.E4M3 else 1.0
+    kc_h, vc_h = host_cache(w, k, v, ks, vs)
     kc, vc = cache_tensors(w)
     fill_device_cache(w, bits_to_dev(k, w.src_dtype), bits_to_dev(v, w.src_dtype), kc, vc, ks, vs)
-    ids, qq, bt, cl = decode_inputs(w, bits_to_dev(q, w.q_dtype))
-    return kc, vc, qq, bt, cl, int(w.context_lens[ids].max()), ks, vs
-
-
-@pytest.mark.parametrize("kv", [workloads.BF16, workloads.E4M3])
-def test_noalloc_matches_workspace_entry_two_calls_in_a_row(kv):
-    # contexts long enough for several 512-token partitions, so the scratch is used
-    w = workloads.independent("noalloc", 61 + kv, [3000, 1, 700, 2600, 1536, 17], 16, 4, 128,
-                              workloads.BF16, kv)
-    kc, vc, qq, bt, cl, max_ctx, ks, vs = _setup(w)
-    assert pkv.decode_workspace_size(qq.shape[0], qq.shape[1], 128, max_ctx) > 0
+    qsl = workloads.query_start_loc(w.q_lens)
+    ids = w.decode_ids()
     tol = TOL_FP8 if kv == workloads.E4M3 else TOL_16BIT
-    q2 = torch.flip(qq, dims=[0]).contiguous()  # a second, different query batch
+    # call 1: every sequence, up to 6 partitions each; call 2: three other
+    # sequences' queries in another order over shorter contexts (at most 3
+    # partitions), rows landing on other slots of the scratch
+    calls = [(list(ids), list(w.context_lens[ids])),
+             ([ids[4], ids[3], ids[0]], [1100, 900, 600])]
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for query in (qq, q2):
+    for sel, lens in calls:
+        sel = np.asarray(sel)
+        lens = np.asarray(lens, np.int32)
+        qh = np.ascontiguousarray(q[qsl[sel]])
+        query = bits_to_dev(qh, w.q_dtype)
+        bt_h = np.ascontiguousarray(w.block_tables[sel])
+        bt = torch.from_numpy(bt_h).cuda()
+        cl = torch.from_numpy(lens).cuda()
+        max_ctx = int(lens.max())
+        assert pkv.decode_workspace_size(len(sel), w.num_heads, 128, max_ctx) > 0
         ref = torch.empty_like(query)
         pkv.paged_attention_decode(ref, query, kc, vc, bt, cl, w.scale, max_context_len=max_ctx,
                                    k_scale=ks, v_scale=vs, device_errors=err)
@@ -56,7 +70,12 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row(kv):
         pkv.paged_attention_decode_noalloc(got, query, kc, vc, bt, cl, w.scale, max_ctx,
                                            k_scale=ks, v_scale=vs, device_errors=err)
         torch.cuda.synchronize()
-        check_close(got.float().cpu().numpy(), ref.float().cpu().numpy(), tol, "noalloc")
+        exact = oracle.paged_attention_decode(qh, kc_h, vc_h, bt_h, lens, w.num_kv_heads,
+                                              w.head_dim, 16, w.num_blocks, w.scale, w.q_dtype,
+                                              w.kv_dtype, ks, vs)
+        g = got.float().cpu().numpy()
+        check_close(g, ref.float().cpu().numpy(), tol, "noalloc vs workspace entry")
+        check_close(g, exact, tol, "noalloc vs oracle")
     assert pkv.check_errors(err) == 0
 
 
