@@ -436,19 +436,32 @@ int pkv_check_errors(uint32_t* device_errors, uint32_t* bits_out, void* stream);
  * Test hook for the failure detection above (the pages have no counterpart:
  * "第34讲 …", §1.2 speaks of preemption and service levels only).  Arms the
  * next attention call made in this process (decode, prefill chunk, draft
- * tree, mixed batch or cascade): in that call's kernel(s) the first copy
- * producer of the first CTA does not issue its skip_copy-th tile copy
+ * tree, mixed batch or cascade): in that call's tensor-core kernel(s) the
+ * first copy producer of the first CTA does not issue its skip_copy-th tile
+ * copy
  * (counted from 1), and every device-side wait is bounded by wait_limit_us
  * microseconds (0: the default of about 2 s) instead of the default.  The
  * waits for the missing tile then run out: the kernel ORs
  * PKV_DEVERR_TIMEOUT into device_errors, lets its issued copies and MMAs
  * finish, releases its tensor memory and returns, and pkv_check_errors then
  * returns PKV_ERR_TIMEOUT.  The rows of that CTA's work are unspecified;
- * later calls are unaffected.  No copy in flight is ever abandoned and no
+ * later calls are unaffected.  A call that runs on the CUDA-core decode
+ * kernel (one query head per KV head, or head_dim 64) takes the hook without
+ * effect: that kernel carries no hook code in its copy loop.  No copy in flight is ever abandoned and no
  * GPU fault is raised.  The hook is taken by exactly one call.
  * PKV_ERR_INVALID_ARG when skip_copy <= 0.
  */
 int pkv_debug_arm_wait_timeout(int skip_copy, unsigned wait_limit_us);
+
+/*
+ * Selects the kernel that runs causal chunks (pkv_paged_attention_prefill_chunk)
+ * and draft trees (pkv_paged_attention_prefill_tree) on tensor cores: 1 pairs
+ * of CTAs that share each 256-row query tile, 0 (the default) one CTA per
+ * 128-row tile.  Both compute the same attention; the switch exists to test
+ * and measure one against the other.  Process-wide; returns the previous
+ * setting, or PKV_ERR_INVALID_ARG for a value other than 0 or 1.
+ */
+int pkv_debug_prefill_pairs(int enable);
 
 /* A static, human-readable name for a pkv_status value. */
 const char* pkv_status_string(int status);

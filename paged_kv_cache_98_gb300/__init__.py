@@ -29,7 +29,7 @@ __all__ = [
     "paged_attention_decode_noalloc", "paged_attention_prefill_chunk", "check_errors", "status_string", "version",
     "paged_attention_prefill_tree", "cascade_workspace_size", "paged_attention_decode_cascade",
     "copy_blocks", "BlockPool", "Request", "mixed_workspace_size", "paged_attention_mixed",
-    "debug_arm_wait_timeout",
+    "debug_arm_wait_timeout", "debug_prefill_pairs",
 ]
 
 F16, BF16, FP8_E4M3 = 0, 1, 2
@@ -96,6 +96,8 @@ def load():
             lib.pkv_check_errors.restype = _I
             lib.pkv_check_errors.argtypes = [_P, _P, _P]
             lib.pkv_debug_arm_wait_timeout.restype = _I
+            lib.pkv_debug_prefill_pairs.restype = _I
+            lib.pkv_debug_prefill_pairs.argtypes = [_I]
             lib.pkv_debug_arm_wait_timeout.argtypes = [_I, ctypes.c_uint]
             lib.pkv_mixed_workspace_size.restype = _SZ
             lib.pkv_mixed_workspace_size.argtypes = [_I] * 5
@@ -533,6 +535,15 @@ def debug_arm_wait_timeout(skip_copy: int, wait_limit_us: int = 0) -> None:
     reports a wait timeout through its error word (pkv_debug_arm_wait_timeout)."""
     _check("pkv_debug_arm_wait_timeout", load().pkv_debug_arm_wait_timeout(skip_copy,
                                                                             wait_limit_us))
+
+
+def debug_prefill_pairs(enable: bool) -> bool:
+    """Causal and draft-tree chunks on CTA pairs (True) or on one CTA per query
+    tile (False, the default); returns the previous setting."""
+    rc = load().pkv_debug_prefill_pairs(1 if enable else 0)
+    if rc < 0:
+        raise PagedKVError("pkv_debug_prefill_pairs", rc)
+    return bool(rc)
 
 
 def check_errors(device_errors, stream=None) -> int:

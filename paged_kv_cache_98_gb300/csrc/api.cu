@@ -107,6 +107,7 @@ namespace pkv {
 
 // The failure-detection test hook armed by pkv_debug_arm_wait_timeout: taken
 // (and cleared) by the next attention call.
+extern std::atomic<int> g_prefill_pairs;  // prefill_tc.cu
 std::atomic<int> g_hook_skip{0};
 std::atomic<unsigned long long> g_hook_limit_ns{0};
 
@@ -508,6 +509,11 @@ int pkv_paged_attention_decode_cascade(void* out, const void* q, const void* k_c
   rc = pkv::launch_paged_decode_tc(ps, q_dtype, kv_dtype, st);
   if (rc != PKV_OK) return rc;
   return pkv::launch_lse_merge(ps, q_dtype, head_dim, st);
+}
+
+int pkv_debug_prefill_pairs(int enable) {
+  if (enable != 0 && enable != 1) return PKV_ERR_INVALID_ARG;
+  return pkv::g_prefill_pairs.exchange(enable);
 }
 
 int pkv_debug_arm_wait_timeout(int skip_copy, unsigned wait_limit_us) {

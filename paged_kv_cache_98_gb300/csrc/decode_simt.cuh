@@ -164,9 +164,6 @@ __global__ void __launch_bounds__(kSimtThreads, 2) paged_attention_simt_kernel(c
       blk = 0;
     }
     const uint8_t* src = (is_v ? p.v_cache : p.k_cache) + ((size_t)blk * p.num_kv_heads + kvh) * TILE;
-    // test hook: this copy is never issued, so the wait for the tile runs out
-    if (p.skip_copy > 0 && u + 1 == p.skip_copy && warp == 0 && row == 0 && kvh == 0 && part == 0)
-      return;
     mbar_arrive_expect_tx(&my_bars[st], TILE);
     bulk_g2s(my_ring + (size_t)st * TILE, src, TILE, &my_bars[st]);
   };
@@ -198,7 +195,7 @@ __global__ void __launch_bounds__(kSimtThreads, 2) paged_attention_simt_kernel(c
   int u = 0;
   for (; u < nw; ++u) {
     const int st = u % STAGES;
-    if (!mbar_wait(&my_bars[st], (u / STAGES) & 1, wait_limit(p))) {
+    if (!mbar_wait(&my_bars[st], (u / STAGES) & 1)) {
       ok = false;
       break;
     }
@@ -275,7 +272,7 @@ __global__ void __launch_bounds__(kSimtThreads, 2) paged_attention_simt_kernel(c
   if (run) {
     for (; u < ntiles; ++u) {
       const int st = u % STAGES;
-      if (!mbar_wait(&my_bars[st], (u / STAGES) & 1, wait_limit(p))) {
+      if (!mbar_wait(&my_bars[st], (u / STAGES) & 1)) {
         ok = false;
         break;
       }

@@ -289,8 +289,8 @@ __device__ __forceinline__ void issue_pv(uint32_t d, uint32_t a, uint64_t dv, ui
 // the four, then each lane's share of the output.  Unit u of F x H x 4 (F
 // such rows): lane quarter u % 4, head (u / 4) % H, row (u / 4) / H.  Keys in
 // a block outside the pool count as zero vectors (the main pass flags them).
-template <class QT, bool kTree>
-__device__ __noinline__ void few_key_rows(const AttnParams& p, const Smem& sm, int first,
+template <class QT, bool kTree, class SM>
+__device__ __noinline__ void few_key_rows(const AttnParams& p, const SM& sm, int first,
                                           int stride) {
   using T = typename QT::T;
   const int H = p.num_heads, S = p.num_seqs;

@@ -66,13 +66,6 @@ def test_tensor_core_decode_wait_runs_out(skip):
     assert run_case(w) > 0  # the device is healthy and the kernel correct afterwards
 
 
-def test_cuda_core_decode_wait_runs_out():
-    # g = 1: the CUDA-core decode kernel
-    w = workloads.independent("timeout-simt", 7102, [900, 33, 1600], 4, 4, 128, F16, F16)
-    _decode_times_out(w, 2)
-    assert run_case(w) > 0
-
-
 def test_tensor_core_prefill_wait_runs_out():
     w = workloads.independent("timeout-pre", 7103, [900, 1500, 300], 16, 4, 128, BF16, BF16,
                               q_lens=[256, 300, 64])
