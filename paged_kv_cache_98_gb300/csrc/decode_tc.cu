@@ -8,18 +8,19 @@ namespace pkv {
 namespace {
 using namespace dec_tc;
 
-template <class QT, bool G16, bool FP8>
+// kH: heads the softmax computes (4 for groups of at most 4, else all rows)
+template <class QT, bool G16, bool FP8, int kH>
 __global__ void __launch_bounds__(tc_threads(G16, FP8), 1)
     paged_decode_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v,
                            const __grid_constant__ CUtensorMap tm_q, int kv_rows) {
   extern __shared__ uint8_t smem_raw[];
-  decode_body<QT, G16, FP8, tc_threads(G16, FP8)>(p, tm_k, tm_v, tm_q, kv_rows, blockIdx.x,
-                                                 gridDim.x, smem_raw);
+  decode_body<QT, G16, FP8, tc_threads(G16, FP8), kH>(p, tm_k, tm_v, tm_q, kv_rows, blockIdx.x,
+                                                     gridDim.x, smem_raw);
 }
 
 // ---- host side ---------------------------------------------------------------------------
-template <class QT, bool G16, bool FP8>
+template <class QT, bool G16, bool FP8, int kH = (G16 ? 16 : 8)>
 int launch_tc_typed(const AttnParams& p, cudaStream_t stream) {
   const bool bf16 = std::is_same<QT, BF16>::value;
   const uint64_t kv_rows = (uint64_t)p.num_blocks * p.num_kv_heads * kBlockSize;
@@ -39,7 +40,7 @@ int launch_tc_typed(const AttnParams& p, cudaStream_t stream) {
                     L::kQHalf % 1024 == 0 && L::kQBytes % 1024 == 0,
                 "swizzled buffers must start on 1024-byte boundaries");
   static_assert(L::kStepKeys * L::kRowBytes == kTailBytes, "tail buffer = one MMA step of V");
-  auto kern = paged_decode_tc_kernel<QT, G16, FP8>;
+  auto kern = paged_decode_tc_kernel<QT, G16, FP8, kH>;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -92,19 +93,23 @@ bool tc_decode_supported(const AttnParams& p, int q_dtype, int kv_dtype, int hea
 }
 
 int launch_paged_decode_tc(const AttnParams& p, int q_dtype, int kv_dtype, cudaStream_t stream) {
-  const bool g16 = p.group > 8;
+  const bool g16 = p.group > 8, g4 = p.group <= 4;
   if (kv_dtype == PKV_FP8_E4M3) {
     if (q_dtype == PKV_BF16)
-      return g16 ? launch_tc_typed<BF16, true, true>(p, stream)
-                 : launch_tc_typed<BF16, false, true>(p, stream);
-    return g16 ? launch_tc_typed<F16, true, true>(p, stream)
-               : launch_tc_typed<F16, false, true>(p, stream);
+      return g16  ? launch_tc_typed<BF16, true, true>(p, stream)
+             : g4 ? launch_tc_typed<BF16, false, true, 4>(p, stream)
+                  : launch_tc_typed<BF16, false, true>(p, stream);
+    return g16  ? launch_tc_typed<F16, true, true>(p, stream)
+           : g4 ? launch_tc_typed<F16, false, true, 4>(p, stream)
+                : launch_tc_typed<F16, false, true>(p, stream);
   }
   if (q_dtype == PKV_BF16)
-    return g16 ? launch_tc_typed<BF16, true, false>(p, stream)
-               : launch_tc_typed<BF16, false, false>(p, stream);
-  return g16 ? launch_tc_typed<F16, true, false>(p, stream)
-             : launch_tc_typed<F16, false, false>(p, stream);
+    return g16  ? launch_tc_typed<BF16, true, false>(p, stream)
+           : g4 ? launch_tc_typed<BF16, false, false, 4>(p, stream)
+                : launch_tc_typed<BF16, false, false>(p, stream);
+  return g16  ? launch_tc_typed<F16, true, false>(p, stream)
+         : g4 ? launch_tc_typed<F16, false, false, 4>(p, stream)
+              : launch_tc_typed<F16, false, false>(p, stream);
 }
 
 }  // namespace pkv

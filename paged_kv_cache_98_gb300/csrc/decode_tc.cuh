@@ -18,10 +18,16 @@
 // the few query heads, fill the M = 128 rows).
 //
 // Warp roles: 0-3 softmax + epilogue (thread = TMEM lane); 4 K producer (and
-// the query on 16-bit caches); 5 TMEM owner + MMA issuer; 6 V producer; then
-// on 16-bit caches 7 the tail loader (and 8-9 second K and V producers with
-// at most 8 heads per group), on E4M3 caches 7-10 the query converters and
-// tail loader.  One warp issuing 16-row boxes moves about 31 GB/s per SM, two
+// the query on 16-bit caches); 5 TMEM owner + issuer of the score MMAs; 6 V
+// producer; then on 16-bit caches 7 the tail loader (and 8-9 second K and V
+// producers with at most 8 heads per group), on E4M3 caches 7-10 the query
+// converters and tail loader.  On 16-bit caches one more warp (the last)
+// issues the P.V MMAs: with the two products issued by separate warps, the K
+// stream (scores of the next items) never waits behind a P.V product that
+// waits for its softmax, and the V stream never waits behind K tiles still in
+// flight (70B-GQA decode 0.209 -> 0.174 ms).  E4M3 caches keep one issuer,
+// running S(i+1) then P.V(i): their softmax warps, not the streams, set the
+// pace, and the extra warp's registers cost more than it returns.  One warp issuing 16-row boxes moves about 31 GB/s per SM, two
 // per ring more, so the 16-bit rings' boxes are spread over two warps where
 // registers allow (the E4M3 kernel is bound by its softmax warps, and second
 // producers bought it nothing).  K and V tiles stream through separate
@@ -67,7 +73,9 @@ namespace {
 // producer warps per ring, and threads: the 16-bit, 16-head variant needs
 // more registers than 320 threads leave
 constexpr int tc_prod(bool g16, bool fp8) { return (fp8 || g16) ? 1 : 2; }
-constexpr int tc_threads(bool g16, bool fp8) { return fp8 ? 352 : (g16 ? 256 : 320); }
+// (16-bit caches: one more warp issues the P.V MMAs, see decode_body)
+constexpr bool tc_split_mma(bool fp8) { return !fp8; }
+constexpr int tc_threads(bool g16, bool fp8) { return fp8 ? 352 : (g16 ? 288 : 352); }
 constexpr int kTileKeys = 128;
 constexpr int kPart = 512;
 constexpr int kTilesPerPart = kPart / kTileKeys;
@@ -130,7 +138,9 @@ struct Smem {
   uint64_t v_fixed[4];   // by (items with a partial block so far) % 4
   uint64_t tail_free[2];  // tail[i] read by the products: by that count % 2
   uint64_t qs_ready[4];  // by item % 4
+  uint64_t s_free[2];    // the softmax has read S of buffer b (item % 2)
   uint64_t mma_done;
+  uint64_t pv_done;
   // per sequence: first (sequence, partition) pair << 9 | (keys of its last
   // partition - 1); entry [S] holds the total << 9
   int seq_pack[kMaxSeqs + 1];
@@ -310,19 +320,24 @@ __device__ __forceinline__ bool all_softmax(bool ok) { return all_of_group<1>(ok
 
 // The kernel body, for kCta threads (at least tc_threads(G16, FP8); warps
 // beyond the roles below only take part in the CTA-wide barriers), running
-// as CTA `cta` of `ncta` that share the items.
-template <class QT, bool G16, bool FP8, int kCta>
+// as CTA `cta` of `ncta` that share the items.  The softmax computes kH heads
+// (at least the group size): 4 for groups of at most 4 query heads, which
+// halves its exponentials, shuffles and P stores against the 8 rows Q and P
+// hold; the rows past kH keep the zeros P starts with.
+template <class QT, bool G16, bool FP8, int kCta, int kH = (G16 ? 16 : 8)>
 __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorMap& tm_k,
                                             const CUtensorMap& tm_v, const CUtensorMap& tm_q,
                                             int kv_rows, int cta, int ncta, uint8_t* smem_raw) {
   static_assert(kCta >= tc_threads(G16, FP8) && kCta <= 384 && kCta % 32 == 0, "CTA size");
   using L = Layout<G16, FP8>;
+  static_assert(kH % 2 == 0 && kH <= L::kRows, "heads of the softmax");
   constexpr int KS = L::kKStages, VS = L::kVStages;
   constexpr int kThreads = kCta;
   constexpr int kProd = tc_prod(G16, FP8);
-  // second producers of the K and V rings
+  // second producers of the K and V rings, and the P.V issuer (the last warp)
   constexpr int kWarpK1 = kProd == 2 ? 8 : -1;
   constexpr int kWarpV1 = kProd == 2 ? 9 : -1;
+  constexpr int kWarpPV = tc_split_mma(FP8) ? tc_threads(G16, FP8) / 32 - 1 : -1;
   Smem<G16, FP8>& sm = *reinterpret_cast<Smem<G16, FP8>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -354,8 +369,12 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
       mbar_init(&sm.v_fixed[i], 1);
       mbar_init(&sm.qs_ready[i], 1);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(&sm.tail_free[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.tail_free[i], 1);
+      mbar_init(&sm.s_free[i], 1);
+    }
     mbar_init(&sm.mma_done, 1);
+    mbar_init(&sm.pv_done, 1);
     sm.abort = 0;
     fence_barrier_init();
   }
@@ -504,10 +523,11 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
       for (uint32_t x = pos > nst ? pos - nst : 0; x < pos; ++x)
         mbar_wait(&full[x % nst], (x / nst) & 1, 10000000ull);
     }
-  } else if (warp == 5) {
-    // ---- MMA issuer ---------------------------------------------------------------------
-    // The whole warp runs the loop (waits, counters and descriptors stay warp-
-    // uniform); one elected lane issues the MMAs and commits.
+  } else if (warp == 5 || warp == kWarpPV) {
+    // ---- MMA issuers: scores (warp 5) and P.V products (the last warp) -------------------
+    // Each warp runs its loop whole (waits, counters and descriptors stay warp-
+    // uniform); one elected lane issues the MMAs and commits (a commit tracks
+    // the MMAs of the thread that issued them).
     {
       const bool leader = tc::elect_one();
       auto commit = [&](uint64_t* bar) {
@@ -520,7 +540,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
       int idx = cta;
       uint32_t kpos = 0, vpos = 0;
       int ntail = 0;  // items with a partial last block so far
-      Item cur, nxt;
+      Item cur;
       int it = 0;
       bool ok = true;
       auto mma_s = [&](const Item& x, int k) -> bool {
@@ -614,22 +634,40 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
         commit(&sm.o_ready[b]);
         return true;
       };
-      bool has = next_item(p, sm, idx, total, cur, ncta);
-      if (has) ok = mma_s(cur, 0);
-      while (has && ok) {
-        const bool has_n = next_item(p, sm, idx, total, nxt, ncta);
-        if (has_n) ok = mma_s(nxt, it + 1);
-        if (ok) ok = mma_pv(cur, it);
-        cur = nxt;
-        has = has_n;
-        ++it;
+      if (!tc_split_mma(FP8)) {
+        // one issuer: S(0), then per item i: S(i+1), P.V(i)
+        Item nxt;
+        bool has = next_item(p, sm, idx, total, cur, ncta);
+        if (has) ok = mma_s(cur, 0);
+        while (has && ok) {
+          const bool has_n = next_item(p, sm, idx, total, nxt, ncta);
+          if (has_n) ok = mma_s(nxt, it + 1);
+          if (ok) ok = mma_pv(cur, it);
+          cur = nxt;
+          has = has_n;
+          ++it;
+        }
+      } else if (warp == 5) {
+        // S of item k goes to TMEM buffer k % 2 once the softmax has read item k - 2's
+        while (ok && next_item(p, sm, idx, total, cur, ncta)) {
+          const int b = it & 1;
+          if (it >= 2) {
+            ok = wait(&sm.s_free[b], ((it - 2) >> 1) & 1);
+            if (ok) tc::fence_after_sync();
+          }
+          if (ok) ok = mma_s(cur, it);
+          ++it;
+        }
+      } else {
+        while (ok && next_item(p, sm, idx, total, cur, ncta)) ok = mma_pv(cur, it++);
       }
       if (!ok && leader) flag_error(p.errors, PKV_DEVERR_TIMEOUT);
       // no MMA of ours may still be running when TMEM is released
-      commit(&sm.mma_done);
-      mbar_wait(&sm.mma_done, 0, 100000000ull);
+      uint64_t* done = warp == 5 ? &sm.mma_done : &sm.pv_done;
+      commit(done);
+      mbar_wait(done, 0, 100000000ull);
     }
-  } else if (warp == 7 || (FP8 && warp > 7)) {
+  } else if (warp == 7 || (FP8 && warp >= 8 && warp <= 10)) {
     // ---- tail loader (16-bit: warp 7) / query converters + tail loader (E4M3: 7-10) -----
     constexpr int kGroup = FP8 ? 128 : 32;
     const int gtid = threadIdx.x - 224;
@@ -835,13 +873,13 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
         if (few) return true;
         OutT* dst = static_cast<OutT*>(p.out) + head0 * kD + d;
 #pragma unroll
-        for (int h = 0; h < L::kRows; ++h)
+        for (int h = 0; h < kH; ++h)
           if (h < p.group) store_out(dst + h * kD, o[h] * sm.stat_inv[b][h]);
       } else if (x.slot < p.max_parts) {
         float* dst = p.o_part + (head0 * p.max_parts + x.slot) * kD + d;
         const size_t stride = (size_t)p.max_parts * kD;
 #pragma unroll
-        for (int h = 0; h < L::kRows; ++h)
+        for (int h = 0; h < kH; ++h)
           if (h < p.group) dst[h * stride] = o[h] * sm.stat_inv[b][h];
         if (d < p.group) p.lse[(head0 + d) * p.max_parts + x.slot] = sm.stat_lse[b][d];
       }
@@ -862,7 +900,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
         ok = all_softmax(wait_bar(&sm.qs_ready[it & 3], (it >> 2) & 1, abort, lim));
         if (!ok) break;
 #pragma unroll
-        for (int h = 0; h < L::kRows; ++h) qsh[h] = qs * sm.qscale[it & 3][h];
+        for (int h = 0; h < kH; ++h) qsh[h] = qs * sm.qscale[it & 3][h];
       }
       float s[kTilesPerPart][16];
       if constexpr (FP8 && G16) {
@@ -889,7 +927,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
 #pragma unroll
           for (int t = 0; t < kTilesPerPart; ++t)
 #pragma unroll
-            for (int h = 0; h < 8; ++h) s[t][h] += s[t][h + 8];
+            for (int h = 0; h < kH; ++h) s[t][h] += s[t][h + 8];
         }
       }
       // Running max per head over this thread's keys, then over the CTA.  All
@@ -899,12 +937,12 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
       // independent shuffle chains of the heads interleave.
       float mx[16];
 #pragma unroll
-      for (int h = 0; h < L::kRows; ++h) mx[h] = -INFINITY;
+      for (int h = 0; h < kH; ++h) mx[h] = -INFINITY;
 #pragma unroll
       for (int t = 0; t < kTilesPerPart; ++t) {
         const bool valid = t < cur.ntiles && t * kTileKeys + tid < cur.n;
 #pragma unroll
-        for (int h = 0; h < L::kRows; ++h) {
+        for (int h = 0; h < kH; ++h) {
           s[t][h] = valid ? s[t][h] * (FP8 ? qsh[h] : qs) : -INFINITY;
           mx[h] = fmaxf(mx[h], s[t][h]);
         }
@@ -912,15 +950,17 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
 #pragma unroll
       for (int o = 16; o; o >>= 1)
 #pragma unroll
-        for (int h = 0; h < L::kRows; ++h) mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], o));
+        for (int h = 0; h < kH; ++h) mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], o));
       if (lane == 0) {
 #pragma unroll
-        for (int h = 0; h < L::kRows; ++h) sm.red_max[warp][h] = mx[h];
+        for (int h = 0; h < kH; ++h) sm.red_max[warp][h] = mx[h];
       }
+      tc::fence_before_sync();
       tc::named_sync(1, 128);
+      if (tc_split_mma(FP8) && tid == 0) mbar_arrive(&sm.s_free[b]);  // S is in registers
       float sum[16];
 #pragma unroll
-      for (int h = 0; h < L::kRows; ++h) {
+      for (int h = 0; h < kH; ++h) {
         sum[h] = 0.0f;
         mx[h] = fmaxf(fmaxf(sm.red_max[0][h], sm.red_max[1][h]),
                       fmaxf(sm.red_max[2][h], sm.red_max[3][h]));
@@ -933,7 +973,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
         if (t < cur.ntiles) {
           const int key = t * kTileKeys + tid;
 #pragma unroll
-          for (int h = 0; h < L::kRows; h += 2) {
+          for (int h = 0; h < kH; h += 2) {
             const float e0 = fast_exp2(s[t][h] - mx[h]);
             const float e1 = fast_exp2(s[t][h + 1] - mx[h + 1]);
             sum[h] += e0;
@@ -965,10 +1005,10 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
 #pragma unroll
       for (int o = 16; o; o >>= 1)
 #pragma unroll
-        for (int h = 0; h < L::kRows; ++h) sum[h] += __shfl_xor_sync(kFull, sum[h], o);
+        for (int h = 0; h < kH; ++h) sum[h] += __shfl_xor_sync(kFull, sum[h], o);
       if (lane == 0) {
 #pragma unroll
-        for (int h = 0; h < L::kRows; ++h) sm.red_sum[warp][h] = sum[h];
+        for (int h = 0; h < kH; ++h) sm.red_sum[warp][h] = sum[h];
       }
       fence_proxy_async_smem();
       tc::fence_before_sync();

@@ -89,7 +89,8 @@ __device__ int split_ctas(const AttnParams& pd, const AttnParams& pp, int forced
   return n < 1 ? 1 : n;
 }
 
-template <class QT>
+// kH: heads the decode softmax computes (4 for groups of at most 4, else 8)
+template <class QT, int kH>
 __global__ void __launch_bounds__(kMixThreads, 1)
     mixed_tc_kernel(const AttnParams pd, const AttnParams pp,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(kMixThreads, 1)
     pre_tc::prefill_body<QT, false, false>(pp, tm_k, tm_v, tm_qp, kv_rows, blockIdx.x, n_pre,
                                            smem_raw);
   else
-    dec_tc::decode_body<QT, false, false, kMixThreads>(pd, tm_k, tm_v, tm_qd, kv_rows,
+    dec_tc::decode_body<QT, false, false, kMixThreads, kH>(pd, tm_k, tm_v, tm_qd, kv_rows,
                                                        blockIdx.x - n_pre, gridDim.x - n_pre,
                                                        smem_raw);
 }
@@ -127,13 +128,14 @@ int launch_mixed_typed(const AttnParams& pd, const AttnParams& pp, int total_q, 
   constexpr size_t smem = (kDecSmem > kPreSmem ? kDecSmem : kPreSmem) + 1024;
   static_assert(smem <= 232448, "shared memory budget of one CTA");
   static_assert(3 * (kMixThreads / 32) * sizeof(long long) <= kPreSmem, "split scratch");
-  auto kern = mixed_tc_kernel<QT>;
-  static bool configured = false;
-  if (!configured) {
+  const bool g4 = pd.group <= 4;
+  auto kern = g4 ? mixed_tc_kernel<QT, 4> : mixed_tc_kernel<QT, 8>;
+  static bool configured[2] = {false, false};
+  if (!configured[g4]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return PKV_ERR_CUDA;
-    configured = true;
+    configured[g4] = true;
   }
   const int grid = sm_count();
   if (grid < 2) return PKV_ERR_UNSUPPORTED;

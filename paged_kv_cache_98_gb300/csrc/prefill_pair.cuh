@@ -116,7 +116,8 @@ __device__ __forceinline__ bool next_pair_item(const AttnParams& p, const PairSm
   return true;
 }
 
-// Bounded wait on a barrier of this CTA that the other CTA may arrive on.
+// Bounded wait, acquiring at cluster scope, for the barrier the other CTA's
+// thread-written tail rows are published on.
 __device__ __forceinline__ bool wait_bar_c(uint64_t* bar, uint32_t parity, volatile int* abort,
                                            unsigned long long limit_ns) {
   if (tc::mbar_test_cluster(bar, parity)) return true;
@@ -327,7 +328,7 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
       bool good = true;
       if (lane == 0) {
         if (pos >= (uint32_t)kPairStages)
-          good = wait_bar_c(&sm.empty[st], ((pos / kPairStages) - 1) & 1, abort, lim);
+          good = wait_bar(&sm.empty[st], ((pos / kPairStages) - 1) & 1, abort, lim);
         if (good && !skip) tc::mbar_arrive_expect_tx_cluster(bar, is_v ? vbytes : kbytes);
       }
       if (!__shfl_sync(kFull, (int)good, 0)) return false;
@@ -349,7 +350,7 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
     // context as zeros, swizzled like the ring (0 * NaN would poison the MMA)
     auto load_tail = [&]() -> bool {
       bool good = true;
-      if (lane == 0 && ntail >= 1) good = wait_bar_c(&sm.tail_free, (ntail - 1) & 1, abort, lim);
+      if (lane == 0 && ntail >= 1) good = wait_bar(&sm.tail_free, (ntail - 1) & 1, abort, lim);
       if (!__shfl_sync(kFull, (int)good, 0)) return false;
       const int bi = (x.ctx - 1) / kBlockSize;
       const int blk = __ldg(p.block_tables + (size_t)x.trow * p.max_blocks_per_seq + bi);
@@ -368,14 +369,14 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive_cluster(at0(&sm.tail_full));
+      if (lane == 0) tc::mbar_arrive_cluster_release(at0(&sm.tail_full));
       ++ntail;
       return true;
     };
     while (ok && next_pair_item(p, sm, idx, total, x, npairs)) {
       bool good = true;
       if (pw == 0 && lane == 0) {
-        if (nitem >= 1) good = wait_bar_c(&sm.q_empty, (nitem - 1) & 1, abort, lim);
+        if (nitem >= 1) good = wait_bar(&sm.q_empty, (nitem - 1) & 1, abort, lim);
         if (good) {
           const int nq = x.nt[1] > 0 ? 2 : 1;
           const uint32_t bar = at0(&sm.q_full);
@@ -432,7 +433,7 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
         }
       };
       auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-        return __shfl_sync(kFull, (int)wait_bar_c(bar, parity, abort, lim), 0) != 0;
+        return __shfl_sync(kFull, (int)wait_bar(bar, parity, abort, lim), 0) != 0;
       };
       int idx = pair;
       uint32_t pos = 0;
@@ -476,7 +477,8 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
       };
       auto tail_wait = [&](int t) -> bool {
         if (t != x.nk - 1 || x.tail_step < 0) return true;
-        const bool r = wait(&sm.tail_full, ntail & 1);
+        const bool r =
+            __shfl_sync(kFull, (int)wait_bar_c(&sm.tail_full, ntail & 1, abort, lim), 0) != 0;
         if (r) tc::fence_after_sync();
         return r;
       };
@@ -559,7 +561,7 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
 #pragma unroll
       for (int i = 0; i < 8; ++i) l8[i] = 0.0f;
       for (int t = 0; t <= x.last[qt]; ++t, ++ns) {
-        ok = all_group(wait_bar_c(&sm.s_ready[qt], ns & 1, abort, lim), qt);
+        ok = all_group(wait_bar(&sm.s_ready[qt], ns & 1, abort, lim), qt);
         if (!ok) break;
         tc::fence_after_sync();
         float sv[kTileKeys];
@@ -649,7 +651,7 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
       }
       if (!ok) break;
       // ---- epilogue: O / l --------------------------------------------------------------
-      ok = all_group(wait_bar_c(&sm.o_done[qt], nit & 1, abort, lim), qt);
+      ok = all_group(wait_bar(&sm.o_done[qt], nit & 1, abort, lim), qt);
       if (!ok) break;
       tc::fence_after_sync();
       const float l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));

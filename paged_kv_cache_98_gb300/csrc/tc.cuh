@@ -281,19 +281,24 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
 }
-// Arrivals (release at cluster scope) on a barrier of either CTA.
+// Arrivals on a barrier of either CTA of the pair (release at CTA scope, as
+// for a local arrival: the data they publish is TMA- or tcgen05-written, ordered
+// by the async proxy or by the tcgen05 fences around the synchronisation).
 __device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
-                   bar),
-               "r"(bytes)
+  asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// An arrival that also publishes this thread's earlier shared-memory writes to
+// the other CTA (release at cluster scope; slower, used once per work item).
+__device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
                : "memory");
 }
-// Phase test of a barrier of this CTA, acquiring at cluster scope (arrivals
-// may come from the other CTA).
+// Phase test of a barrier of this CTA, acquiring at cluster scope (pairs with
+// mbar_arrive_cluster_release).
 __device__ __forceinline__ bool mbar_test_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
