@@ -167,6 +167,13 @@ __device__ __forceinline__ void flag_error(uint32_t* errors, uint32_t bits) {
   if (errors) atomicOr(errors, bits);
 }
 
+// max(a, b, c) in one instruction (three-input max of sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // 2^x with the hardware approximation (relative error about 2^-22; inputs
 // below -126 give 0).  Softmax weights are rounded to 16 bits afterwards.
 __device__ __forceinline__ float fast_exp2(float x) {

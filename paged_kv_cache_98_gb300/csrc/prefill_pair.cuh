@@ -557,9 +557,9 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
           kTree && valid ? __ldg(p.tree_mask + x.q0 + x.t0[qt] + tok) : 0ull;
       const int first_pos = x.pos0[qt] + tok_off;  // this CTA's first row's position
       float m_run = -INFINITY;
-      float l8[8];
+      float2 l2[4];  // partial row sums (independent chains, packed pairs)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) l8[i] = 0.0f;
+      for (int i = 0; i < 4; ++i) l2[i] = make_float2(0.0f, 0.0f);
       for (int t = 0; t <= x.last[qt]; ++t, ++ns) {
         ok = all_group(wait_bar(&sm.s_ready[qt], ns & 1, abort, lim), qt);
         if (!ok) break;
@@ -605,7 +605,7 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < kTileKeys; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
+          for (int c = 0; c < kTileKeys; c += 2) mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], sv[c], sv[c + 1]);
         }
         const float mt =
             fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
@@ -617,20 +617,12 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
           alpha = t == 0 ? 0.0f : fast_exp2(m_run - mt);
           m_run = mt;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) l8[i] *= alpha;
+          for (int i = 0; i < 4; ++i) l2[i] = __fmul2_rn(l2[i], make_float2(alpha, alpha));
         }
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           float pk[16];
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int k0 = h * 32 + 2 * c;
-            const float e0 = fast_exp2(fmaf(sv[k0], qa, -m_run));
-            const float e1 = fast_exp2(fmaf(sv[k0 + 1], qa, -m_run));
-            l8[(2 * c) & 7] += e0;
-            l8[(2 * c + 1) & 7] += e1;
-            pk[c] = __uint_as_float(pack2<QT>(e0, e1));
-          }
+          exp_pairs<QT>(sv + h * 32, qa, m_run, l2, pk);
           tc::tmem_st16(s_col + 16 * h, pk);
         }
         if (t > 0 && __any_sync(kFull, need)) {
@@ -654,7 +646,8 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
       ok = all_group(wait_bar(&sm.o_done[qt], nit & 1, abort, lim), qt);
       if (!ok) break;
       tc::fence_after_sync();
-      const float l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+      const float l = ((l2[0].x + l2[0].y) + (l2[1].x + l2[1].y)) +
+                      ((l2[2].x + l2[2].y) + (l2[3].x + l2[3].y));
       const float inv = valid ? 1.0f / l : 0.0f;
       OutT* orow = static_cast<OutT*>(p.out) + head * kD;
       const bool store = valid && !(kTree ? cbase < kFewKeys : qpos < kFewKeys);

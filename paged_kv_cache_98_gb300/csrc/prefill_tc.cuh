@@ -246,6 +246,22 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   }
 }
 
+// Softmax weights of 32 keys of a row (sv[0..31]) as 16 packed 16-bit pairs,
+// with their sums added to the row's partial sums: x = s * qa - m on packed
+// fp32 pairs (one rounding, as fmaf), 2^x on the MUFU.  Each pair's weights go
+// to sums l2[c % 4], the same chains as unpacked code would use.
+template <class QT>
+__device__ __forceinline__ void exp_pairs(const float* sv, float qa, float m, float2* l2,
+                                          float* pk) {
+  const float2 qa2 = make_float2(qa, qa), nm2 = make_float2(-m, -m);
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const float e0 = fast_exp2(fmaf(sv[2 * c], qa, -m)), e1 = fast_exp2(fmaf(sv[2 * c + 1], qa, -m));
+    l2[c & 3] = __fadd2_rn(l2[c & 3], make_float2(e0, e1));
+    pk[c] = __uint_as_float(pack2<QT>(e0, e1));
+  }
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]^T, 16-bit operands: A is M lanes x K
 // elements, two elements per 32-bit column (the lower half holds the even one).
 __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
@@ -812,9 +828,9 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
       const uint64_t tmask =
           kTree && valid ? __ldg(p.tree_mask + x.q0 + x.t0[qt] + tok) : 0ull;
       float m_run = -INFINITY;
-      float l8[8];  // partial row sums (independent chains)
+      float2 l2[4];  // partial row sums (independent chains, packed pairs)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) l8[i] = 0.0f;
+      for (int i = 0; i < 4; ++i) l2[i] = make_float2(0.0f, 0.0f);
       for (int t = x.first[qt]; t <= x.last[qt]; t += x.step, ++ns) {
         ok = all_group(wait_bar(&sm.s_ready[qt], ns & 1, abort, lim), qt);
         if (!ok) break;
@@ -861,7 +877,7 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < kTileKeys; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
+          for (int c = 0; c < kTileKeys; c += 2) mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], sv[c], sv[c + 1]);
         }
         const float mt =
             fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
@@ -874,21 +890,13 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
           alpha = (t == x.first[qt]) ? 0.0f : fast_exp2(m_run - mt);
           m_run = mt;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) l8[i] *= alpha;
+          for (int i = 0; i < 4; ++i) l2[i] = __fmul2_rn(l2[i], make_float2(alpha, alpha));
         }
         // P over the first 64 columns of S: keys 2c and 2c+1 in column c
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           float pk[16];
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int k0 = h * 32 + 2 * c;
-            const float e0 = fast_exp2(fmaf(sv[k0], qa, -m_run));
-            const float e1 = fast_exp2(fmaf(sv[k0 + 1], qa, -m_run));
-            l8[(2 * c) & 7] += e0;
-            l8[(2 * c + 1) & 7] += e1;
-            pk[c] = __uint_as_float(pack2<QT>(e0, e1));
-          }
+          exp_pairs<QT>(sv + h * 32, qa, m_run, l2, pk);
           tc::tmem_st16(s_col + 16 * h, pk);
         }
         // the product of tile t adds onto O: rescale it first when a row's max moved
@@ -913,7 +921,8 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
       ok = all_group(wait_bar(&sm.o_done[qt], nit & 1, abort, lim), qt);
       if (!ok) break;
       tc::fence_after_sync();
-      const float l = ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+      const float l = ((l2[0].x + l2[0].y) + (l2[1].x + l2[1].y)) +
+                      ((l2[2].x + l2[2].y) + (l2[3].x + l2[3].y));
       const float inv = valid ? 1.0f / l : 0.0f;
       OutT* orow = static_cast<OutT*>(p.out) + head * kD;
       // shared-prefix mode: the normalised partial and its log-sum-exp (base 2,
