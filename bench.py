@@ -311,7 +311,8 @@ class GpuStep:
         elif len(self.dec):
             n += 1 + (1 if self.parts > 1 else 0)
         if len(self.pre):
-            n += 1 + (1 if -(-self.max_ctx_pre // 512) > 1 else 0)
+            # the tensor-core chunk kernel (after the query split on E4M3 caches)
+            n += 1 + (1 if self.w.kv_dtype == 2 else 0)
         return n
 
     def write(self):
@@ -880,7 +881,8 @@ def other_workloads(dev, peak, barrier):
 
     import workloads
     out = {}
-    for name, steps in (("gqa70b_shared", 200), ("long_fp8", 100), ("mixed", 100)):
+    for name, steps in (("gqa70b_shared", 200), ("long_fp8", 100), ("mixed", 100),
+                        ("mixed_fp8", 100)):
         w = workloads.NAMED[name]()
         st = GpuStep(w, dev)
         res = st.timed(steps, 5, barrier)
@@ -910,7 +912,7 @@ def other_workloads(dev, peak, barrier):
             d["cascade_GBps_logical"] = round(kvb / (cms * 1e-3) / 1e9, 1)
             d["cascade_GBps_unique"] = round(ub / (cms * 1e-3) / 1e9, 1)
             d["cascade_speedup"] = round(res["decode_ms"] / cms, 3)
-        if name == "mixed":
+        if name == "mixed":  # (E4M3 caches have no fused kernel)
             # the same batch's attention in one fused call
             fms = st.fused_timed(steps, 5)
             d["fused_attention_ms"] = round(fms, 5)

@@ -179,7 +179,10 @@ int pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_c
                                        void* stream);
 
 /*
- * Bytes of device workspace pkv_paged_attention_prefill_chunk needs.
+ * Bytes of device workspace pkv_paged_attention_prefill_chunk needs (256-byte
+ * aligned when passed): the larger of the CUDA-core path's split-K partials
+ * and, for head_dim 128, the tensor-core path's split query of an E4M3-cache
+ * call (two E4M3 bytes and one fp32 scale per query row and head).
  */
 size_t pkv_prefill_workspace_size(int total_q, int num_heads, int head_dim,
                                   int max_context_len, int max_q_len);
@@ -199,6 +202,12 @@ size_t pkv_prefill_workspace_size(int total_q, int num_heads, int head_dim,
  *   The query at row query_start_loc[s] + i sits at absolute position
  *   pos = context_lens[s] - q_len_s + i and attends keys 0..pos.
  *   max_q_len        an upper bound of every q_len_s (sizes the launch).
+ *   workspace        at least pkv_prefill_workspace_size(...) bytes, 256-byte
+ *                    aligned; may be NULL for 16-bit caches at head_dim 128
+ *                    with num_heads / num_kv_heads dividing 128 (the
+ *                    tensor-core kernel), which need none.  E4M3 caches on
+ *                    that kernel split the query into it (PKV_ERR_WORKSPACE
+ *                    when it is missing or short).
  *   Other arguments as for pkv_paged_attention_decode.
  */
 int pkv_paged_attention_prefill_chunk(void* out, const void* q, const void* k_cache,
@@ -455,13 +464,16 @@ int pkv_debug_arm_wait_timeout(int skip_copy, unsigned wait_limit_us);
 
 /*
  * Selects the kernel that runs causal chunks (pkv_paged_attention_prefill_chunk)
- * and draft trees (pkv_paged_attention_prefill_tree) on tensor cores: 1 pairs
- * of CTAs that share each 256-row query tile, 0 (the default) one CTA per
- * 128-row tile.  Both compute the same attention; the switch exists to test
- * and measure one against the other.  Process-wide; returns the previous
- * setting, or PKV_ERR_INVALID_ARG for a value other than 0 or 1.
+ * and draft trees (pkv_paged_attention_prefill_tree) on tensor cores:
+ *   1  pairs of CTAs that share each 256-row query tile (each CTA loads half of
+ *      every K/V tile);
+ *   0  one CTA per 128-row tile;
+ *   2  (the default) pairs for draft trees, one CTA per tile for causal chunks.
+ * All compute the same attention, bit for bit; the switch exists to test and
+ * measure one against the other.  Process-wide; returns the previous setting,
+ * or PKV_ERR_INVALID_ARG for another value.
  */
-int pkv_debug_prefill_pairs(int enable);
+int pkv_debug_prefill_pairs(int mode);
 
 /* A static, human-readable name for a pkv_status value. */
 const char* pkv_status_string(int status);

@@ -537,13 +537,14 @@ def debug_arm_wait_timeout(skip_copy: int, wait_limit_us: int = 0) -> None:
                                                                             wait_limit_us))
 
 
-def debug_prefill_pairs(enable: bool) -> bool:
-    """Causal and draft-tree chunks on CTA pairs (True) or on one CTA per query
-    tile (False, the default); returns the previous setting."""
-    rc = load().pkv_debug_prefill_pairs(1 if enable else 0)
+def debug_prefill_pairs(mode: int) -> int:
+    """Kernel for causal and draft-tree chunks: 1 CTA pairs, 0 one CTA per
+    query tile, 2 (the default) pairs for draft trees only; returns the
+    previous setting (pkv_debug_prefill_pairs)."""
+    rc = load().pkv_debug_prefill_pairs(int(mode))
     if rc < 0:
         raise PagedKVError("pkv_debug_prefill_pairs", rc)
-    return bool(rc)
+    return rc
 
 
 def check_errors(device_errors, stream=None) -> int:

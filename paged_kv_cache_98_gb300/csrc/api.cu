@@ -223,8 +223,11 @@ size_t pkv_prefill_workspace_size(int total_q, int num_heads, int head_dim, int 
                                   int max_q_len) {
   (void)max_q_len;
   if (total_q <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
-  return split_workspace((size_t)total_q, num_heads, head_dim,
-                         parts_for(max_context_len, kDefaultPartition));
+  // CUDA-core path: split-K partials; E4M3 caches on tensor cores: the split query
+  const size_t simt = split_workspace((size_t)total_q, num_heads, head_dim,
+                                      parts_for(max_context_len, kDefaultPartition));
+  const size_t q8 = head_dim == 128 ? pkv::prefill_q8_bytes(total_q, num_heads) : 0;
+  return simt > q8 ? simt : q8;
 }
 
 int pkv_paged_attention_prefill_chunk(void* out, const void* q, const void* k_cache,
@@ -269,6 +272,9 @@ int pkv_paged_attention_prefill_chunk(void* out, const void* q, const void* k_ca
     p.q_scale = scale * pkv::kLog2e * (fp8 ? k_scale : 1.0f);
     p.v_scale = fp8 ? v_scale : 1.0f;
     pkv::take_debug_hook(p);
+    if (fp8)
+      return pkv::launch_prefill_tc_fp8(p, q_dtype, total_q, workspace, workspace_bytes,
+                                        static_cast<cudaStream_t>(stream));
     return pkv::launch_prefill_tc(p, q_dtype, total_q, static_cast<cudaStream_t>(stream));
   }
   const size_t need = split_workspace((size_t)total_q, num_heads, head_dim, p.max_parts);
@@ -313,8 +319,11 @@ int pkv_paged_attention_prefill_tree(void* out, const void* q, const void* k_cac
   p.max_parts = parts_for(max_context_len, kDefaultPartition);
   if (p.max_parts > 16384) return PKV_ERR_UNSUPPORTED;
   p.errors = device_errors;
-  // the tensor-core prefill kernel carries the mask; other shapes are unsupported
-  if (!pkv::tc_prefill_supported(p, q_dtype, kv_dtype, head_dim)) return PKV_ERR_UNSUPPORTED;
+  // the tensor-core prefill kernel carries the mask; other shapes (and E4M3
+  // caches, whose query split needs a workspace this call does not take) are
+  // unsupported
+  if (kv_dtype != q_dtype || !pkv::tc_prefill_supported(p, q_dtype, kv_dtype, head_dim))
+    return PKV_ERR_UNSUPPORTED;
   p.q_scale = scale * pkv::kLog2e;
   p.v_scale = 1.0f;
   pkv::take_debug_hook(p);
@@ -511,9 +520,9 @@ int pkv_paged_attention_decode_cascade(void* out, const void* q, const void* k_c
   return pkv::launch_lse_merge(ps, q_dtype, head_dim, st);
 }
 
-int pkv_debug_prefill_pairs(int enable) {
-  if (enable != 0 && enable != 1) return PKV_ERR_INVALID_ARG;
-  return pkv::g_prefill_pairs.exchange(enable);
+int pkv_debug_prefill_pairs(int mode) {
+  if (mode < 0 || mode > 2) return PKV_ERR_INVALID_ARG;
+  return pkv::g_prefill_pairs.exchange(mode);
 }
 
 int pkv_debug_arm_wait_timeout(int skip_copy, unsigned wait_limit_us) {

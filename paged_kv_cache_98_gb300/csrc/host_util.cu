@@ -58,6 +58,21 @@ bool make_map_e4m3(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// E4M3 q viewed as [tokens][heads][128 B]: boxes of 128 columns x box_heads
+// heads x box_tokens tokens (token-major rows of 128 bytes), 128-byte swizzle.
+bool make_map_q3d_e4m3(CUtensorMap* m, const void* base, uint64_t tokens, uint32_t heads,
+                       uint32_t box_heads, uint32_t box_tokens) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {128, heads, (cuuint64_t)tokens};
+  cuuint64_t strides[2] = {128, (cuuint64_t)heads * 128};
+  cuuint32_t box[3] = {128, box_heads, box_tokens};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // q viewed as [tokens][heads][128]: boxes of 64 columns x box_heads heads x
 // box_tokens tokens, 128-byte swizzle (the box lands as box_heads*box_tokens
 // rows of 128 bytes, token-major).

@@ -57,6 +57,9 @@ struct AttnParams {
   // counted from 1), so that the waits for that tile run out.
   unsigned long long wait_limit_ns;
   int skip_copy;
+  // Prefill on E4M3 caches: per (query row, head) scale s of the split query
+  // (q / s = hi + lo, both E4M3), [rows][num_heads]; null otherwise.
+  const float* q8_scale;
 };
 
 // Limit of the launch's device-side waits.
@@ -93,6 +96,11 @@ int launch_paged_decode_tc(const AttnParams& p, int q_dtype, int kv_dtype, cudaS
 // tcgen05 chunked-prefill attention (head_dim 128, 16-bit caches, 128 % g == 0).
 bool tc_prefill_supported(const AttnParams& p, int q_dtype, int kv_dtype, int head_dim);
 int launch_prefill_tc(const AttnParams& p, int q_dtype, int total_q, cudaStream_t stream);
+// Device bytes the E4M3-cache prefill needs for its split query (0 otherwise).
+size_t prefill_q8_bytes(int total_q, int num_heads);
+// The E4M3-cache prefill: splits q into the workspace, then launches the kernel.
+int launch_prefill_tc_fp8(const AttnParams& p, int q_dtype, int total_q, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
 
 // One launch for a mixed batch: pd describes the decode rows (as for
 // launch_paged_decode_tc), pp the prefill chunks (as for launch_prefill_tc);
@@ -109,6 +117,8 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, bool bf16, uin
 bool make_map_q3d(CUtensorMap* m, const void* base, uint64_t tokens, uint32_t heads, bool bf16,
                   uint32_t box_heads, uint32_t box_tokens);
 bool make_map_e4m3(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows);
+bool make_map_q3d_e4m3(CUtensorMap* m, const void* base, uint64_t tokens, uint32_t heads,
+                       uint32_t box_heads, uint32_t box_tokens);
 int sm_count();
 
 int launch_lse_merge(const AttnParams& p, int q_dtype, int head_dim, cudaStream_t stream);

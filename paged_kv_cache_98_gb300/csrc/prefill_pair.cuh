@@ -605,7 +605,8 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < kTileKeys; c += 2) mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], sv[c], sv[c + 1]);
+          for (int c = 0; c < kTileKeys; c += 2)
+            mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], sv[c], sv[c + 1]);
         }
         const float mt =
             fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),

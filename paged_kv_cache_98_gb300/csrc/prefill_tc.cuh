@@ -75,6 +75,8 @@ constexpr int kTileKeys = 128;
 constexpr int kRowsM = 128;
 constexpr int kStages = 4;     // ring stages (5 in shared-prefix mode: q[0] joins the ring)
 constexpr int kMaxStages = 5;
+constexpr int kStages8 = 8;    // E4M3 caches: tiles of 16 KB, eight in the same ring
+constexpr int kRingBars = 8;   // barriers for the deepest ring
 constexpr int kTileBytes = 128 * kD * 2;  // 32 KB: [2 halves][128 rows][128 B]
 constexpr int kHalf = kTileBytes / 2;
 constexpr int kTailBytes = kBlockSize * kD * 2;  // one block of V: [2 halves][16 rows][128 B]
@@ -82,6 +84,11 @@ constexpr int kMaxSeqs = 1024;
 constexpr int kTmemCols = 512;  // S/P a, S/P b, O a, O b
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleAt = 8.0f;
+// E4M3 weights: P holds 16 w with w <= 2^4 (the running max moves once a tile
+// exceeds it by 4), so P stays below E4M3's largest value (448) while weights
+// down to 2^-13 keep a code.
+constexpr float kRescaleAt8 = 4.0f;
+constexpr float kPScale8 = 16.0f;
 // Causal rows that see at most this many keys are recomputed in fp32 on the
 // CUDA cores after the main loop: with so few keys the 16-bit rounding of the
 // softmax weights (relative 2^-9 each) does not average out.
@@ -99,8 +106,8 @@ struct Smem {
   int few_start[kMaxSeqs + 1];  // prefix of rows seeing at most kFewKeys keys
   int scan[kThreads / 32];
   int scan2[kThreads / 32];
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
+  uint64_t full[kRingBars];
+  uint64_t empty[kRingBars];
   uint64_t q_full;
   uint64_t q_empty;
   uint64_t s_ready[2];  // per query tile
@@ -138,7 +145,8 @@ __device__ __forceinline__ int key_chunks(const AttnParams& p, int ctx) {
   return (tiles + per - 1) / per;
 }
 
-template <bool kAlt>
+// kFP8: E4M3 caches, whose P.V MMAs take 32 keys per step (16 for 16-bit).
+template <bool kAlt, bool kFP8 = false>
 __device__ __forceinline__ bool next_item(const AttnParams& p, const Smem& sm, int& idx,
                                           int total, Item& it, int stride) {
   if (idx >= total) return false;
@@ -178,7 +186,7 @@ __device__ __forceinline__ bool next_item(const AttnParams& p, const Smem& sm, i
   }
   const bool partial = (it.ctx & (kBlockSize - 1)) != 0;
   it.tail_step = partial && (it.ctx - 1) / kTileKeys == it.nk - 1
-                     ? ((it.ctx - 1) % kTileKeys) / kBlockSize
+                     ? ((it.ctx - 1) % kTileKeys) / (kFP8 ? 2 * kBlockSize : kBlockSize)
                      : -1;
   it.step = alt ? 2 : 1;
 #pragma unroll
@@ -262,6 +270,25 @@ __device__ __forceinline__ void exp_pairs(const float* sv, float qa, float m, fl
   }
 }
 
+// The same for E4M3 weights: 32 keys (sv[0..31]) as 8 columns of four E4M3
+// codes of kPScale8 * 2^x, sums of the unrounded weights.
+__device__ __forceinline__ void exp_quads8(const float* sv, float qa, float m, float2* l2,
+                                           float* pk) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    float e[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) e[i] = fast_exp2(fmaf(sv[4 * c + i], qa, -m));
+    l2[(2 * c) & 3] = __fadd2_rn(l2[(2 * c) & 3], make_float2(e[0], e[1]));
+    l2[(2 * c + 1) & 3] = __fadd2_rn(l2[(2 * c + 1) & 3], make_float2(e[2], e[3]));
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(
+        make_float2(e[0] * kPScale8, e[1] * kPScale8), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(
+        make_float2(e[2] * kPScale8, e[3] * kPScale8), __NV_SATFINITE, __NV_E4M3);
+    pk[c] = __uint_as_float(lo | (hi << 16));
+  }
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]^T, 16-bit operands: A is M lanes x K
 // elements, two elements per 32-bit column (the lower half holds the even one).
 __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
@@ -297,6 +324,43 @@ __device__ __forceinline__ void issue_pv(uint32_t d, uint32_t a, uint64_t dv, ui
   }
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, 8-bit operands (kind::f8f6f4): A is M
+// lanes x K elements, four elements per 32-bit column.
+__device__ __forceinline__ void mma_f8_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// E4M3 caches.  Scores: S = Q_hi K^T + Q_lo K^T, with the query split per row
+// as q / s = hi + lo (E4M3 each, [128 rows][128 B] apiece, lo 16 KB after hi)
+// and K [128 keys][128 B]; K-steps of 32 dims.
+__device__ __forceinline__ void issue_scores8(uint32_t d, uint64_t dq, uint64_t dk, uint32_t idesc) {
+#pragma unroll
+  for (int part = 0; part < 2; ++part) {
+#pragma unroll
+    for (int kk = 0; kk < kD / 32; ++kk)
+      tc::mma_f8(d, dq + (uint64_t)((part * (kTileBytes / 2) + kk * 32) >> 4),
+                 dk + (uint64_t)((kk * 32) >> 4), idesc, (part | kk) != 0);
+  }
+}
+
+// O (+)= P V with P as E4M3 in TMEM (32 keys per 8 columns) and V [128 keys][128
+// B] (MN-major, one swizzle atom wide), 32 keys per step; step ts (if >= 0)
+// takes its V rows from the tail buffer.
+__device__ __forceinline__ void issue_pv8(uint32_t d, uint32_t a, uint64_t dv, uint64_t dtail,
+                                          int ts, uint32_t acc0, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < kTileKeys / 32; ++kk) {
+    const uint64_t b = kk == ts ? dtail : dv + (uint64_t)((kk * (32 * 128)) >> 4);
+    mma_f8_tmem_a(d, a + kk * 8, b, idesc, acc0 | (kk != 0 ? 1u : 0u));
+  }
+}
+
 // kTree: draft-tree mode (per-row ancestor masks over the chunk's keys);
 // kAlt: shared-prefix mode (non-causal, key chunks, partial outputs)
 // The rows that see few keys (few_rows), recomputed in fp32 from the caches
@@ -305,9 +369,11 @@ __device__ __forceinline__ void issue_pv(uint32_t d, uint32_t a, uint64_t dv, ui
 // the four, then each lane's share of the output.  Unit u of F x H x 4 (F
 // such rows): lane quarter u % 4, head (u / 4) % H, row (u / 4) / H.  Keys in
 // a block outside the pool count as zero vectors (the main pass flags them).
-template <class QT, bool kTree, class SM>
+// kFP8: E4M3 caches (codes decoded; k_scale is in q_scale, v_scale applied).
+template <class QT, bool kTree, class SM, bool kFP8 = false>
 __device__ __noinline__ void few_key_rows(const AttnParams& p, const SM& sm, int first,
                                           int stride) {
+  constexpr int kElem = kFP8 ? 1 : 2;
   using T = typename QT::T;
   const int H = p.num_heads, S = p.num_seqs;
   const int lane = threadIdx.x & 31;
@@ -344,14 +410,17 @@ __device__ __noinline__ void few_key_rows(const AttnParams& p, const SM& sm, int
       if (kTree && j >= prior && !((tmask >> (j - prior)) & 1ull)) continue;
       const int blk = __ldg(p.block_tables + (size_t)trow * p.max_blocks_per_seq + j / kBlockSize);
       const bool bok = blk >= 0 && blk < p.num_blocks;
-      const size_t off = (((size_t)(bok ? blk : 0) * p.num_kv_heads + kvh) * kBlockSize +
-                          j % kBlockSize) * kD + quarter * 32;
+      const size_t off = ((((size_t)(bok ? blk : 0) * p.num_kv_heads + kvh) * kBlockSize +
+                           j % kBlockSize) * kD + quarter * 32) * kElem;
       float kv[32];
       float dot = 0.0f;
       if (bok) {
-        const uint4* kp = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.k_cache) + off);
+        const uint4* kp = reinterpret_cast<const uint4*>(p.k_cache + off);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) to_float(__ldg(kp + c), kv + 8 * c, QT());
+        for (int c = 0; c < 32 * kElem / 16; ++c) {
+          if constexpr (kFP8) to_float(__ldg(kp + c), kv + 16 * c, E4M3());
+          else to_float(__ldg(kp + c), kv + 8 * c, QT());
+        }
 #pragma unroll
         for (int d = 0; d < 32; ++d) dot = fmaf(qf[d], kv[d], dot);
       }
@@ -368,14 +437,17 @@ __device__ __noinline__ void few_key_rows(const AttnParams& p, const SM& sm, int
       const float w = exp2f(sc - m);
       l += w;
       if (bok) {
-        const uint4* vp = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(p.v_cache) + off);
+        const uint4* vp = reinterpret_cast<const uint4*>(p.v_cache + off);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) to_float(__ldg(vp + c), kv + 8 * c, QT());
+        for (int c = 0; c < 32 * kElem / 16; ++c) {
+          if constexpr (kFP8) to_float(__ldg(vp + c), kv + 16 * c, E4M3());
+          else to_float(__ldg(vp + c), kv + 8 * c, QT());
+        }
 #pragma unroll
         for (int d = 0; d < 32; ++d) acc[d] = fmaf(w, kv[d], acc[d]);
       }
     }
-    const float inv = 1.0f / l;
+    const float inv = p.v_scale / l;
     uint4* op = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + ((size_t)row * H + h) * kD +
                                          quarter * 32);
 #pragma unroll
@@ -391,21 +463,31 @@ __device__ __noinline__ void few_key_rows(const AttnParams& p, const SM& sm, int
 }
 
 // The kernel body, run as CTA `cta` of `ncta` that share the items.
-template <class QT, bool kTree, bool kAlt>
+// kFP8: E4M3 caches (not with kAlt).  K and V tiles are [128 keys][128 B] (16
+// KB, one box per block), eight to the ring; the query comes split per row as
+// q / s = hi + lo in E4M3 (rows of hi, then the same rows of lo, at token
+// offset num_rows in tm_q; s in p.q8_scale); scores are S = (Q_hi + Q_lo) K^T
+// on 8-bit MMAs, scaled by s and k_scale in the softmax; P is E4M3 of
+// kPScale8 w in TMEM, O = P V on 8-bit MMAs, divided by kPScale8 l and
+// multiplied by v_scale.
+template <class QT, bool kTree, bool kAlt, bool kFP8 = false>
 __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensorMap& tm_k,
                                              const CUtensorMap& tm_v, const CUtensorMap& tm_q,
                                              int kv_rows, int cta, int ncta, uint8_t* smem_raw) {
+  static_assert(!(kFP8 && kAlt), "E4M3 caches have no shared-prefix mode");
+  constexpr int kStageBytes = kFP8 ? kTileBytes / 2 : kTileBytes;
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr uint32_t kAB = std::is_same<QT, BF16>::value ? 1u : 0u;
-  constexpr uint32_t kIdescS = tc::idesc_f16(kAB, 0, 0, 128, 128);
-  constexpr uint32_t kIdescO = tc::idesc_f16(kAB, 0, 1, 128, 128);
+  // kind::f16 (0 f16, 1 bf16) or, on E4M3 caches, kind::f8f6f4 (0 = E4M3)
+  constexpr uint32_t kIdescS = tc::idesc_f16(kFP8 ? 0u : kAB, 0, 0, 128, 128);
+  constexpr uint32_t kIdescO = tc::idesc_f16(kFP8 ? 0u : kAB, 0, 1, 128, 128);
   const int g = p.group;
 
   // ---- set-up ---------------------------------------------------------------------------
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kMaxStages; ++s) {
+    for (int s = 0; s < kRingBars; ++s) {
       mbar_init(&sm.full[s], kProducers);
       mbar_init(&sm.empty[s], 1);
     }
@@ -514,7 +596,7 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
     const int mine = (8 - pw + kProducers - 1) / kProducers;  // blocks per tile: 3, 3, 2
     const bool my_lane = (lane & 7) % kProducers == pw;
     constexpr bool alt = kAlt;  // shared-prefix mode
-    constexpr int nst = alt ? kMaxStages : kStages;
+    constexpr int nst = kFP8 ? kStages8 : (alt ? kMaxStages : kStages);
     uint8_t* const ring = &sm.ring[0][0];  // stage 4 (shared-prefix mode) is q[0]
     int idx = cta;
     uint32_t pos = 0;
@@ -542,14 +624,14 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
       bool good = true;
       if (lane == 0) {
         if (pos >= (uint32_t)nst) good = wait_bar(&sm.empty[st], ((pos / nst) - 1) & 1, abort, lim);
-        if (good && !skip) mbar_arrive_expect_tx(&sm.full[st], mine * (kTileBytes / 8));
+        if (good && !skip) mbar_arrive_expect_tx(&sm.full[st], mine * (kStageBytes / 8));
       }
       if (!__shfl_sync(kFull, (int)good, 0)) return false;
       if (!skip && (lane >> 3) == (t & 3) && my_lane) {
-        uint8_t* dst = ring + (size_t)st * kTileBytes + (lane & 7) * (kBlockSize * 128);
+        uint8_t* dst = ring + (size_t)st * kStageBytes + (lane & 7) * (kBlockSize * 128);
         const CUtensorMap* map = is_v ? &tm_v : &tm_k;
         tc::tma_load_2d(dst, map, 0, row, &sm.full[st]);
-        tc::tma_load_2d(dst + kHalf, map, 64, row, &sm.full[st]);
+        if (!kFP8) tc::tma_load_2d(dst + kHalf, map, 64, row, &sm.full[st]);
       }
       __syncwarp();
       ++pos;
@@ -561,20 +643,41 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
       bool good = true;
       if (lane == 0 && ntail >= 1) good = wait_bar(&sm.tail_free, (ntail - 1) & 1, abort, lim);
       if (!__shfl_sync(kFull, (int)good, 0)) return false;
-      const int bi = (x.ctx - 1) / kBlockSize;
-      const int blk = __ldg(p.block_tables + (size_t)x.trow * p.max_blocks_per_seq + bi);
-      const bool bok = blk >= 0 && blk < p.num_blocks;
-      const uint8_t* src =
-          p.v_cache + ((size_t)(bok ? blk : 0) * p.num_kv_heads + x.kvh) * kBlockSize * (kD * 2);
-      const int rows = x.ctx - bi * kBlockSize;
+      if constexpr (kFP8) {
+        // the 32 rows of the MMA step that holds the partial block, [32][128 B]
+        const int key0 = (x.nk - 1) * kTileKeys + x.tail_step * 2 * kBlockSize;
 #pragma unroll
-      for (int i = 0; i < kTailBytes / 16 / 32; ++i) {
-        const int c = lane + 32 * i;
-        const int r = c >> 4, ch = c & 15;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (bok && r < rows) v = __ldg(reinterpret_cast<const uint4*>(src + r * (kD * 2)) + ch);
-        *reinterpret_cast<uint4*>(&sm.tail[0] + (ch >> 3) * (kTailBytes / 2) + r * 128 +
-                                  (((ch & 7) ^ (r & 7)) << 4)) = v;
+        for (int i = 0; i < kTailBytes / 16 / 32; ++i) {
+          const int c = lane + 32 * i;
+          const int r = c >> 3, ch = c & 7;
+          const int key = key0 + r;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (key < x.ctx) {
+            const int blk =
+                __ldg(p.block_tables + (size_t)x.trow * p.max_blocks_per_seq + key / kBlockSize);
+            if (blk >= 0 && blk < p.num_blocks)
+              v = __ldg(reinterpret_cast<const uint4*>(
+                            p.v_cache + (((size_t)blk * p.num_kv_heads + x.kvh) * kBlockSize +
+                                         (key & (kBlockSize - 1))) * kD) + ch);
+          }
+          *reinterpret_cast<uint4*>(&sm.tail[0] + r * 128 + ((ch ^ (r & 7)) << 4)) = v;
+        }
+      } else {
+        const int bi = (x.ctx - 1) / kBlockSize;
+        const int blk = __ldg(p.block_tables + (size_t)x.trow * p.max_blocks_per_seq + bi);
+        const bool bok = blk >= 0 && blk < p.num_blocks;
+        const uint8_t* src =
+            p.v_cache + ((size_t)(bok ? blk : 0) * p.num_kv_heads + x.kvh) * kBlockSize * (kD * 2);
+        const int rows = x.ctx - bi * kBlockSize;
+#pragma unroll
+        for (int i = 0; i < kTailBytes / 16 / 32; ++i) {
+          const int c = lane + 32 * i;
+          const int r = c >> 4, ch = c & 15;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (bok && r < rows) v = __ldg(reinterpret_cast<const uint4*>(src + r * (kD * 2)) + ch);
+          *reinterpret_cast<uint4*>(&sm.tail[0] + (ch >> 3) * (kTailBytes / 2) + r * 128 +
+                                    (((ch & 7) ^ (r & 7)) << 4)) = v;
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -582,7 +685,7 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
       ++ntail;
       return true;
     };
-    while (ok && next_item<kAlt>(p, sm, idx, total, x, ncta)) {
+    while (ok && next_item<kAlt, kFP8>(p, sm, idx, total, x, ncta)) {
       bool good = true;
       if (pw == 0 && lane == 0) {
         if (nitem >= 1) good = wait_bar(&sm.q_empty, (nitem - 1) & 1, abort, lim);
@@ -593,8 +696,14 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
           for (int qt = 0; qt < nq; ++qt) {
             uint8_t* dq = &sm.q[alt ? 1 : qt][0];
             const int tok = x.q0 + x.t0[qt];
-            tc::tma_load_3d(dq, &tm_q, 0, x.kvh * g, tok, &sm.q_full);
-            tc::tma_load_3d(dq + kHalf, &tm_q, 64, x.kvh * g, tok, &sm.q_full);
+            if constexpr (kFP8) {
+              // E4M3 hi rows, then the lo rows (num_rows tokens further on)
+              tc::tma_load_3d(dq, &tm_q, 0, x.kvh * g, tok, &sm.q_full);
+              tc::tma_load_3d(dq + kHalf, &tm_q, 0, x.kvh * g, p.num_rows + tok, &sm.q_full);
+            } else {
+              tc::tma_load_3d(dq, &tm_q, 0, x.kvh * g, tok, &sm.q_full);
+              tc::tma_load_3d(dq + kHalf, &tm_q, 64, x.kvh * g, tok, &sm.q_full);
+            }
           }
         }
       }
@@ -666,7 +775,7 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
       const uint32_t qaddr[2] = {smem_u32(&sm.q[0][0]), smem_u32(&sm.q[1][0])};
       const uint32_t taddr = smem_u32(&sm.tail[0]);
       constexpr bool alt = kAlt;  // shared-prefix mode
-      constexpr int nst = alt ? kMaxStages : kStages;
+      constexpr int nst = kFP8 ? kStages8 : (alt ? kMaxStages : kStages);
       auto acquire = [&](int& st) -> bool {
         st = pos % nst;
         const bool r = wait(&sm.full[st], (pos / nst) & 1);
@@ -680,13 +789,18 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
       const uint64_t dq[2] = {tc::smem_desc(qaddr[alt ? 1 : 0], 16, 1024, tc::kLayoutSw128),
                               tc::smem_desc(qaddr[1], 16, 1024, tc::kLayoutSw128)};
       const uint64_t dk0 = tc::smem_desc(smem_u32(&sm.ring[0][0]), 16, 1024, tc::kLayoutSw128);
-      const uint64_t dv0 =
-          tc::smem_desc(smem_u32(&sm.ring[0][0]), kHalf, 1024, tc::kLayoutSw128);
-      const uint64_t dtail = tc::smem_desc(taddr, kTailBytes / 2, 1024, tc::kLayoutSw128);
+      // V: 16-bit [2 halves][128 keys][128 B] (MN-major, the halves kHalf apart);
+      // E4M3 [128 keys][128 B], one swizzle atom wide
+      const uint64_t dv0 = tc::smem_desc(smem_u32(&sm.ring[0][0]), kFP8 ? 16 : kHalf, 1024,
+                                         tc::kLayoutSw128);
+      const uint64_t dtail =
+          tc::smem_desc(taddr, kFP8 ? 16 : kTailBytes / 2, 1024, tc::kLayoutSw128);
       auto mma_s = [&](int qt, int st) {
-        if (leader)
-          issue_scores(tmem + qt * 128, qt ? dq[1] : dq[0],
-                       dk0 + (uint64_t)(st * (kTileBytes >> 4)), kIdescS);
+        if (leader) {
+          const uint64_t dk = dk0 + (uint64_t)(st * (kStageBytes >> 4));
+          if constexpr (kFP8) issue_scores8(tmem + qt * 128, qt ? dq[1] : dq[0], dk, kIdescS);
+          else issue_scores(tmem + qt * 128, qt ? dq[1] : dq[0], dk, kIdescS);
+        }
         commit(&sm.s_ready[qt]);
       };
       auto mma_pv = [&](int qt, int st, int t) -> bool {
@@ -696,10 +810,16 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
             !wait(&sm.o_free[qt], (nit[qt] - 1) & 1))
           return false;  // the previous item's O has been read out
         tc::fence_after_sync();
-        if (leader)
-          issue_pv(tmem + kColO + qt * 128, tmem + qt * 128,
-                   dv0 + (uint64_t)(st * (kTileBytes >> 4)), dtail,
-                   t == x.nk - 1 ? x.tail_step : -1, t != x.first[qt], kIdescO);
+        if (leader) {
+          const uint64_t dv = dv0 + (uint64_t)(st * (kStageBytes >> 4));
+          const int ts = t == x.nk - 1 ? x.tail_step : -1;
+          if constexpr (kFP8)
+            issue_pv8(tmem + kColO + qt * 128, tmem + qt * 128, dv, dtail, ts, t != x.first[qt],
+                      kIdescO);
+          else
+            issue_pv(tmem + kColO + qt * 128, tmem + qt * 128, dv, dtail, ts, t != x.first[qt],
+                     kIdescO);
+        }
         if (t == x.last[qt]) commit(&sm.o_done[qt]);
         return true;
       };
@@ -738,7 +858,7 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
         }
         return true;
       };
-      while (ok && next_item<kAlt>(p, sm, idx, total, x, ncta)) {
+      while (ok && next_item<kAlt, kFP8>(p, sm, idx, total, x, ncta)) {
         const bool ha = x.last[0] >= 0;
         const bool hb = x.last[1] >= 0;
         int kst = 0, vst = 0;
@@ -803,7 +923,7 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
     uint32_t ns = 0, nit = 0;  // S tiles and items of this query tile
     bool ok = true;
     Item x;
-    while (ok && next_item<kAlt>(p, sm, idx, total, x, ncta)) {
+    while (ok && next_item<kAlt, kFP8>(p, sm, idx, total, x, ncta)) {
       const int tok = tid / g;  // token within the tile
       // rows past the tile's tokens compute on whatever Q holds there; their
       // output is never stored
@@ -823,6 +943,8 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
         continue;
       }
       const int qpos = x.pos0[qt] + (kAlt ? 0 : tok);
+      // E4M3 caches: the row's query scale s (q / s = hi + lo) joins the score scale
+      const float qa_r = kFP8 ? qa * (valid ? __ldg(p.q8_scale + head) : 1.0f) : qa;
       // draft-tree mode: the row's visible chunk keys, from the chunk's first position
       const int cbase = x.pos0[qt] - x.t0[qt];
       const uint64_t tmask =
@@ -877,14 +999,15 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < kTileKeys; c += 2) mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], sv[c], sv[c + 1]);
+          for (int c = 0; c < kTileKeys; c += 2)
+            mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], sv[c], sv[c + 1]);
         }
         const float mt =
             fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * qa;
+                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * qa_r;
         // move the running max (and rescale O) only on a large increase; O is
         // complete up to tile t-1 (S of tile t was issued after its product)
-        const bool need = mt > m_run + kRescaleAt;
+        const bool need = mt > m_run + (kFP8 ? kRescaleAt8 : kRescaleAt);
         float alpha = 1.0f;
         if (need) {
           alpha = (t == x.first[qt]) ? 0.0f : fast_exp2(m_run - mt);
@@ -892,12 +1015,23 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
 #pragma unroll
           for (int i = 0; i < 4; ++i) l2[i] = __fmul2_rn(l2[i], make_float2(alpha, alpha));
         }
-        // P over the first 64 columns of S: keys 2c and 2c+1 in column c
+        if constexpr (kFP8) {
+          // P over the first 32 columns of S: keys 4c .. 4c + 3 in column c
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          float pk[16];
-          exp_pairs<QT>(sv + h * 32, qa, m_run, l2, pk);
-          tc::tmem_st16(s_col + 16 * h, pk);
+          for (int h = 0; h < 2; ++h) {
+            float pk[16];
+            exp_quads8(sv + h * 64, qa_r, m_run, l2, pk);
+            exp_quads8(sv + h * 64 + 32, qa_r, m_run, l2, pk + 8);
+            tc::tmem_st16(s_col + 16 * h, pk);
+          }
+        } else {
+          // P over the first 64 columns of S: keys 2c and 2c+1 in column c
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            float pk[16];
+            exp_pairs<QT>(sv + h * 32, qa_r, m_run, l2, pk);
+            tc::tmem_st16(s_col + 16 * h, pk);
+          }
         }
         // the product of tile t adds onto O: rescale it first when a row's max moved
         if (t > x.first[qt] && __any_sync(kFull, need)) {
@@ -923,7 +1057,8 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
       tc::fence_after_sync();
       const float l = ((l2[0].x + l2[0].y) + (l2[1].x + l2[1].y)) +
                       ((l2[2].x + l2[2].y) + (l2[3].x + l2[3].y));
-      const float inv = valid ? 1.0f / l : 0.0f;
+      // (E4M3: P held kPScale8 w, and V its codes: v_scale / (kPScale8 l))
+      const float inv = valid ? (kFP8 ? p.v_scale / (kPScale8 * l) : 1.0f / l) : 0.0f;
       OutT* orow = static_cast<OutT*>(p.out) + head * kD;
       // shared-prefix mode: the normalised partial and its log-sum-exp (base 2,
       // scaled units), in the warpgroup's slot of the chunk
@@ -963,7 +1098,7 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
     }
     if (!ok && tid == 0) flag_error(p.errors, PKV_DEVERR_TIMEOUT);
     if constexpr (!kAlt) {
-      if (ok) few_key_rows<QT, kTree>(p, sm, cta * 256 + qt * 128 + tid, ncta * 256);
+      if (ok) few_key_rows<QT, kTree, Smem, kFP8>(p, sm, cta * 256 + qt * 128 + tid, ncta * 256);
     }
   }
 

@@ -23,7 +23,7 @@ def _library():
     from paged_kv_cache_98_gb300 import _build
     _build.build()
     pkv.load()
-    prev = pkv.debug_prefill_pairs(False)
+    prev = pkv.debug_prefill_pairs(0)
     yield
     pkv.debug_prefill_pairs(prev)
 
@@ -31,7 +31,7 @@ def _library():
 def _both(w, call):
     """call(out) on the device state of w, with pairs and with single CTAs."""
     outs = []
-    for pairs in (True, False):
+    for pairs in (1, 0):
         pkv.debug_prefill_pairs(pairs)
         outs.append(call())
     return outs
@@ -116,7 +116,7 @@ def test_pairs_wait_runs_out():
     q, kc_h, vc_h, kc, vc, qd, bt, cl, qsl = _state(w)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = torch.empty_like(qd)
-    pkv.debug_prefill_pairs(True)
+    pkv.debug_prefill_pairs(1)
     pkv.debug_arm_wait_timeout(3, 20000)
     pkv.paged_attention_prefill_chunk(out, qd, kc, vc, bt, cl, qsl, w.scale, max_q_len=300,
                                       max_context_len=1300, device_errors=err)

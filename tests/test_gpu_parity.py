@@ -192,6 +192,17 @@ def test_prefill_chunks(g):
     run_case(w)
 
 
+@pytest.mark.parametrize("g,qd", [(1, BF16), (2, F16), (4, BF16), (8, BF16), (16, F16)])
+def test_prefill_chunks_e4m3_cache(g, qd):
+    """Chunks over an E4M3 cache on the tensor-core prefill (8-bit MMAs over a
+    query split into two E4M3 terms): partial last blocks, a chunk longer than
+    one query tile, a single-token chunk, chunks from position 0."""
+    ctx = [40, 17, 64, 600, 700, 1200, 33]
+    qlen = [40, 5, 33, 512, 1, 300, 33]
+    w = workloads.independent("prefill-e4m3", 3200 + g, ctx, 2 * g, 2, 128, qd, E4M3, q_lens=qlen)
+    run_case(w)
+
+
 @pytest.mark.parametrize("seed,g,dt", [(0, 4, BF16), (1, 8, F16), (2, 2, BF16), (3, 4, F16)])
 def test_prefill_from_position_zero(seed, g, dt):
     """Whole prompts as chunks (no prior context): the first rows see one to a

@@ -308,15 +308,21 @@ def gqa70b_shared(seed: int = 2, num_seqs: int = 128, group: int = 3) -> Workloa
 
 
 def mixed(seed: int = 3, num_decode: int = 32, num_prefill: int = 4, chunk: int = 512,
-          prior: int = 2048) -> Workload:
+          prior: int = 2048, kv_dtype: int = BF16) -> Workload:
     """Mixed chunked-prefill batch: 32 decode sequences (context U[1024, 8192]) and
     4 prefill chunks of 512 queries over 2048 prior tokens; 32 q / 8 kv heads,
-    head_dim 128, bf16.  The decode sequences come first."""
+    head_dim 128, bf16 (the cache in kv_dtype).  The decode sequences come first."""
     r = rng(seed)
     dctx = r.integers(1024, 8193, size=num_decode)
     ctx = np.concatenate([dctx, np.full(num_prefill, prior + chunk)])
     q_lens = np.concatenate([np.ones(num_decode, np.int64), np.full(num_prefill, chunk)])
-    return independent("mixed chunked-prefill", seed, ctx, 32, 8, 128, BF16, BF16, q_lens=q_lens)
+    name = "mixed chunked-prefill" + (", e4m3 cache" if kv_dtype == E4M3 else "")
+    return independent(name, seed, ctx, 32, 8, 128, BF16, kv_dtype, q_lens=q_lens)
+
+
+def mixed_fp8(seed: int = 3) -> Workload:
+    """The mixed chunked-prefill batch over an E4M3 cache (per-tensor scales)."""
+    return mixed(seed, kv_dtype=E4M3)
 
 
 def long_fp8(seed: int = 4, num_seqs: int = 8, context: int = 131072) -> Workload:
@@ -344,6 +350,7 @@ NAMED = {
     "llama2_7b_x16": llama2_7b_x16,
     "gqa70b_shared": gqa70b_shared,
     "mixed": mixed,
+    "mixed_fp8": mixed_fp8,
     "long_fp8": long_fp8,
     "long_fp8_x2": long_fp8_x2,
 }
