@@ -463,28 +463,15 @@ __device__ __noinline__ void few_key_rows(const AttnParams& p, const SM& sm, int
 }
 
 // The kernel body, run as CTA `cta` of `ncta` that share the items.
-// kFP8: E4M3 caches (not with kAlt).  K and V tiles are [128 keys][128 B] (16
-// KB, one box per block), eight to the ring; the query comes split per row as
-// q / s = hi + lo in E4M3 (rows of hi, then the same rows of lo, at token
-// offset num_rows in tm_q; s in p.q8_scale); scores are S = (Q_hi + Q_lo) K^T
-// on 8-bit MMAs, scaled by s and k_scale in the softmax; P is E4M3 of
-// kPScale8 w in TMEM, O = P V on 8-bit MMAs, divided by kPScale8 l and
-// multiplied by v_scale.
-template <class QT, bool kTree, bool kAlt, bool kFP8 = false>
-__device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensorMap& tm_k,
-                                             const CUtensorMap& tm_v, const CUtensorMap& tm_q,
-                                             int kv_rows, int cta, int ncta, uint8_t* smem_raw) {
-  static_assert(!(kFP8 && kAlt), "E4M3 caches have no shared-prefix mode");
-  constexpr int kStageBytes = kFP8 ? kTileBytes / 2 : kTileBytes;
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                      ~uintptr_t(1023));
+// Barriers, tensor memory, and the per-sequence tables (query length,
+// context, first query row, the prefix of work units, the prefix of rows
+// recomputed in fp32) of a prefill launch; ends with the CTA synchronised.
+template <bool kTree, bool kAlt>
+__device__ __forceinline__ void prefill_setup(const AttnParams& p, Smem& sm,
+                                              const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                              const CUtensorMap& tm_q) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr uint32_t kAB = std::is_same<QT, BF16>::value ? 1u : 0u;
-  // kind::f16 (0 f16, 1 bf16) or, on E4M3 caches, kind::f8f6f4 (0 = E4M3)
-  constexpr uint32_t kIdescS = tc::idesc_f16(kFP8 ? 0u : kAB, 0, 0, 128, 128);
-  constexpr uint32_t kIdescO = tc::idesc_f16(kFP8 ? 0u : kAB, 0, 1, 128, 128);
   const int g = p.group;
-
   // ---- set-up ---------------------------------------------------------------------------
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRingBars; ++s) {
@@ -584,12 +571,21 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tmem = sm.tmem_base;
-  volatile int* abort = &sm.abort;
-  const unsigned long long lim = wait_limit(p);
-  const int total = sm.seq_start[p.num_seqs] * p.num_kv_heads;
+}
 
-  if (warp >= 9) {
+// The TMA producer warps (9..11) of a prefill launch: per work item the query
+// tile(s), then per key tile its K boxes, the tail rows of V where the tile
+// holds the context's partial last block, and its V boxes, into the ring.
+template <bool kAlt, bool kFP8>
+__device__ __forceinline__ void prefill_producers(const AttnParams& p, Smem& sm,
+                                                  const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                                  const CUtensorMap& tm_q, int kv_rows, int cta,
+                                                  int ncta, int total, volatile int* abort,
+                                                  unsigned long long lim) {
+  constexpr int kStageBytes = kFP8 ? kTileBytes / 2 : kTileBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = p.group;
+  {
     // ---- TMA producers (ring order K0, V0, K1, V1, ...) -----------------------------------
     // Producer pw issues the boxes of blocks j with j % 3 == pw of every tile.
     const int pw = warp - 9;
@@ -747,6 +743,39 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
       for (uint32_t y = pos > (uint32_t)nst ? pos - nst : 0; y < pos; ++y)
         mbar_wait(&sm.full[y % nst], (y / nst) & 1, 10000000ull);
     }
+  }
+}
+
+// kFP8: E4M3 caches (not with kAlt).  K and V tiles are [128 keys][128 B] (16
+// KB, one box per block), eight to the ring; the query comes split per row as
+// q / s = hi + lo in E4M3 (rows of hi, then the same rows of lo, at token
+// offset num_rows in tm_q; s in p.q8_scale); scores are S = (Q_hi + Q_lo) K^T
+// on 8-bit MMAs, scaled by s and k_scale in the softmax; P is E4M3 of
+// kPScale8 w in TMEM, O = P V on 8-bit MMAs, divided by kPScale8 l and
+// multiplied by v_scale.
+template <class QT, bool kTree, bool kAlt, bool kFP8 = false>
+__device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensorMap& tm_k,
+                                             const CUtensorMap& tm_v, const CUtensorMap& tm_q,
+                                             int kv_rows, int cta, int ncta, uint8_t* smem_raw) {
+  static_assert(!(kFP8 && kAlt), "E4M3 caches have no shared-prefix mode");
+  constexpr int kStageBytes = kFP8 ? kTileBytes / 2 : kTileBytes;
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr uint32_t kAB = std::is_same<QT, BF16>::value ? 1u : 0u;
+  // kind::f16 (0 f16, 1 bf16) or, on E4M3 caches, kind::f8f6f4 (0 = E4M3)
+  constexpr uint32_t kIdescS = tc::idesc_f16(kFP8 ? 0u : kAB, 0, 0, 128, 128);
+  constexpr uint32_t kIdescO = tc::idesc_f16(kFP8 ? 0u : kAB, 0, 1, 128, 128);
+  const int g = p.group;
+
+  prefill_setup<kTree, kAlt>(p, sm, tm_k, tm_v, tm_q);
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort = &sm.abort;
+  const unsigned long long lim = wait_limit(p);
+  const int total = sm.seq_start[p.num_seqs] * p.num_kv_heads;
+
+  if (warp >= 9) {
+    prefill_producers<kAlt, kFP8>(p, sm, tm_k, tm_v, tm_q, kv_rows, cta, ncta, total, abort, lim);
   } else if (warp == 8) {
     // ---- MMA issuer --------------------------------------------------------------------
     // Order per item: S_a(0), S_b(0), then for each key tile t:

@@ -29,10 +29,10 @@ def _library():
 
 
 def _both(w, call):
-    """call(out) on the device state of w, with pairs and with single CTAs."""
+    """call() on the device state of w with CTA pairs and with one CTA per tile."""
     outs = []
-    for pairs in (1, 0):
-        pkv.debug_prefill_pairs(pairs)
+    for mode in (1, 0):
+        pkv.debug_prefill_pairs(mode)
         outs.append(call())
     return outs
 
