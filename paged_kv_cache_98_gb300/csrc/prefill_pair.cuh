@@ -29,7 +29,8 @@
 //
 // Barriers.  The even CTA's warp 8 issues every MMA and waits on its own
 // CTA's barriers: full[stage] (3 producers x 2 CTAs arrive, both CTAs' bytes),
-// q_full, tail_full, p_ready and o_free (one arrival per CTA).  Each MMA
+// q_full, tail_full, p_ready and o_free (one arrival per softmax warp of each
+// CTA).  Each MMA
 // commit that releases a resource (empty, q_empty, tail_free) or publishes a
 // result (s_ready, o_done) arrives on that barrier in both CTAs.  The odd
 // CTA's warp 8 only allocates and frees its TMEM with the pair.
@@ -191,9 +192,9 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
     mbar_init(&sm.q_empty, 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(&sm.s_ready[x], 1);
-      mbar_init(&sm.p_ready[x], 2);
+      mbar_init(&sm.p_ready[x], 8);  // one arrival per softmax warp of each CTA
       mbar_init(&sm.o_done[x], 1);
-      mbar_init(&sm.o_free[x], 2);
+      mbar_init(&sm.o_free[x], 8);
     }
     mbar_init(&sm.tail_full, 2);
     mbar_init(&sm.tail_free, 1);
@@ -456,6 +457,11 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
         if (r) tc::fence_after_sync();
         return r;
       };
+      // has the next ring stage landed? (a test, no wait)
+      auto landed = [&]() -> bool {
+        return __shfl_sync(kFull, (int)mbar_peek(&sm.full[pos % kPairStages],
+                                                  (pos / kPairStages) & 1), 0) != 0;
+      };
       auto mma_s = [&](int qt, int st) {
         if (leader)
           issue_scores_pair(tmem + qt * 128, dq[qt], dk0 + (uint64_t)(st * (kHalfTile >> 4)),
@@ -499,11 +505,15 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
           const bool more = t + 1 < x.nk;
           ok = acquire(vst);
           if (ok) ok = tail_wait(t);
-          if (ok && t <= x.last[0]) ok = mma_pv(0, vst, t);
-          if (ok && more) {
+          // K(t + 1) is taken before P_a(t) is awaited when it has landed
+          bool k_taken = false;
+          if (ok && more && landed()) {
             ok = acquire(kst);
-            if (ok && t + 1 <= x.last[0]) mma_s(0, kst);
+            k_taken = true;
           }
+          if (ok && t <= x.last[0]) ok = mma_pv(0, vst, t);
+          if (ok && more && !k_taken) ok = acquire(kst);
+          if (ok && more && t + 1 <= x.last[0]) mma_s(0, kst);
           if (ok && hb) ok = mma_pv(1, vst, t);
           if (!ok) break;
           commit2(&sm.empty[vst]);
@@ -544,24 +554,28 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
     uint32_t ns = 0, nit = 0;
     Item x;
     while (ok && next_pair_item(p, sm, idx, total, x, npairs)) {
-      if (x.last[qt] < 0) continue;  // no tile b in this item
+      // this warpgroup's fields of the item, in registers
+      const int nt = qt ? x.nt[1] : x.nt[0];
+      const int t0 = qt ? x.t0[1] : x.t0[0];
+      const int pos0 = qt ? x.pos0[1] : x.pos0[0];
+      const int last = qt ? x.last[1] : x.last[0];
+      if (last < 0) continue;  // no tile b in this item
       const int tok = tok_off + tid / g;  // token within the pair tile
       // rows past the tile's tokens compute on whatever Q holds there; their
       // output is never stored
-      const bool valid = tok < x.nt[qt];
-      const size_t head =
-          (size_t)(x.q0 + x.t0[qt] + tok) * p.num_heads + (size_t)x.kvh * g + tid % g;
-      const int qpos = x.pos0[qt] + tok;
-      const int cbase = x.pos0[qt] - x.t0[qt];  // the chunk's first position
-      const uint64_t tmask =
-          kTree && valid ? __ldg(p.tree_mask + x.q0 + x.t0[qt] + tok) : 0ull;
-      const int first_pos = x.pos0[qt] + tok_off;  // this CTA's first row's position
+      const bool valid = tok < nt;
+      const size_t head = (size_t)(x.q0 + t0 + tok) * p.num_heads + (size_t)x.kvh * g + tid % g;
+      const int qpos = pos0 + tok;
+      const int cbase = pos0 - t0;  // the chunk's first position
+      const uint64_t tmask = kTree && valid ? __ldg(p.tree_mask + x.q0 + t0 + tok) : 0ull;
+      const int first_pos = pos0 + tok_off;  // this CTA's first row's position
       float m_run = -INFINITY;
       float2 l2[4];  // partial row sums (independent chains, packed pairs)
 #pragma unroll
       for (int i = 0; i < 4; ++i) l2[i] = make_float2(0.0f, 0.0f);
-      for (int t = 0; t <= x.last[qt]; ++t, ++ns) {
-        ok = all_group(wait_bar(&sm.s_ready[qt], ns & 1, abort, lim), qt);
+      // each warp waits and signals on its own: no barrier across the warpgroup
+      for (int t = 0; t <= last; ++t, ++ns) {
+        ok = __all_sync(kFull, wait_bar(&sm.s_ready[qt], ns & 1, abort, lim));
         if (!ok) break;
         tc::fence_after_sync();
         float sv[kTileKeys];
@@ -639,12 +653,12 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
         }
         tc::tmem_wait_st();
         tc::fence_before_sync();
-        tc::named_sync(1 + qt, 128);
-        if (tid == 0) tc::mbar_arrive_cluster(p_ready0);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_cluster(p_ready0);
       }
       if (!ok) break;
       // ---- epilogue: O / l --------------------------------------------------------------
-      ok = all_group(wait_bar(&sm.o_done[qt], nit & 1, abort, lim), qt);
+      ok = __all_sync(kFull, wait_bar(&sm.o_done[qt], nit & 1, abort, lim));
       if (!ok) break;
       tc::fence_after_sync();
       const float l = ((l2[0].x + l2[0].y) + (l2[1].x + l2[1].y)) +
@@ -671,11 +685,11 @@ __device__ __forceinline__ void prefill_pair_body(const AttnParams& p, const CUt
         }
       }
       tc::fence_before_sync();
-      tc::named_sync(1 + qt, 128);
-      if (tid == 0) tc::mbar_arrive_cluster(o_free0);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_cluster(o_free0);
       ++nit;
     }
-    if (!ok && tid == 0) flag_error(p.errors, PKV_DEVERR_TIMEOUT);
+    if (!ok && lane == 0) flag_error(p.errors, PKV_DEVERR_TIMEOUT);
     if (ok) few_key_rows<QT, kTree>(p, sm, blockIdx.x * 256 + qt * 128 + tid, gridDim.x * 256);
   }
 

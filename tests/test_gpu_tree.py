@@ -68,22 +68,29 @@ def test_random_draft_trees(g, dt):
     run_tree(w, np.concatenate(masks))
 
 
-def test_chain_equals_causal_chunk():
-    """A chain-shaped tree is the causal chunk: the same arithmetic, so the same
-    bytes, and both meet the tolerance against the oracle."""
-    qlens = [64, 30]
-    w = workloads.independent("tree-chain", 70, [600, 95], 16, 2, 128, BF16, BF16, q_lens=qlens)
-    masks = np.concatenate([workloads.tree_mask(np.arange(n) - 1) for n in qlens])
-    out_t, ref = run_tree(w, masks)
-    k, v, q = workloads.values_cpu(w)
-    kc, vc = cache_tensors(w)
-    fill_device_cache(w, bits_to_dev(k, BF16), bits_to_dev(v, BF16), kc, vc)
-    qq, bt, cl, qsl_d = all_inputs(w, bits_to_dev(q, BF16))
-    out_c = torch.empty_like(qq)
-    pkv.paged_attention_prefill_chunk(out_c, qq, kc, vc, bt, cl, qsl_d, w.scale,
-                                      max_q_len=64, max_context_len=600)
-    check_close(out_c.float().cpu().numpy(), ref, tol(w), "causal chunk")
-    assert torch.equal(out_t.view(torch.int16), out_c.view(torch.int16))
+@pytest.mark.parametrize("pairs", [1, 0])
+def test_chain_equals_causal_chunk(pairs):
+    """A chain-shaped tree is the causal chunk: on the same kernel (CTA pairs,
+    or one CTA per tile) the same arithmetic, so the same bytes, and both meet
+    the tolerance against the oracle."""
+    prev = pkv.debug_prefill_pairs(pairs)
+    try:
+        qlens = [64, 30]
+        w = workloads.independent("tree-chain", 70, [600, 95], 16, 2, 128, BF16, BF16,
+                                  q_lens=qlens)
+        masks = np.concatenate([workloads.tree_mask(np.arange(n) - 1) for n in qlens])
+        out_t, ref = run_tree(w, masks)
+        k, v, q = workloads.values_cpu(w)
+        kc, vc = cache_tensors(w)
+        fill_device_cache(w, bits_to_dev(k, BF16), bits_to_dev(v, BF16), kc, vc)
+        qq, bt, cl, qsl_d = all_inputs(w, bits_to_dev(q, BF16))
+        out_c = torch.empty_like(qq)
+        pkv.paged_attention_prefill_chunk(out_c, qq, kc, vc, bt, cl, qsl_d, w.scale,
+                                          max_q_len=64, max_context_len=600)
+        check_close(out_c.float().cpu().numpy(), ref, tol(w), "causal chunk")
+        assert torch.equal(out_t.view(torch.int16), out_c.view(torch.int16))
+    finally:
+        pkv.debug_prefill_pairs(prev)
 
 
 def test_unsupported_and_invalid():
