@@ -707,16 +707,22 @@ __device__ __forceinline__ void prefill_producers(const AttnParams& p, Smem& sm,
       // Block rows of the 32-block table chunks (4 key tiles each) the tiles
       // being issued fall in: two chunks cached (K runs a tile ahead of V in
       // shared-prefix mode), the next one read ahead.
-      int rc_c[2] = {-1, -1}, rc_row[2] = {kv_rows, kv_rows};
+      // (two named slots rather than an array: a runtime index would put them
+      // in local memory)
+      int rc_c0 = -1, rc_c1 = -1, rc_row0 = kv_rows, rc_row1 = kv_rows;
       int pre_c = x.kt0 >> 2, pre_raw = fetch(pre_c);
       auto row_for = [&](int t) -> int {
         const int c = t >> 2;
-        if (rc_c[0] == c) return rc_row[0];
-        if (rc_c[1] == c) return rc_row[1];
+        if (rc_c0 == c) return rc_row0;
+        if (rc_c1 == c) return rc_row1;
         const int r = to_row(pre_c == c ? pre_raw : fetch(c));
-        const int sl = rc_c[0] < rc_c[1] ? 0 : 1;  // replace the older chunk
-        rc_c[sl] = c;
-        rc_row[sl] = r;
+        if (rc_c0 < rc_c1) {  // replace the older chunk
+          rc_c0 = c;
+          rc_row0 = r;
+        } else {
+          rc_c1 = c;
+          rc_row1 = r;
+        }
         pre_c = c + 1;
         pre_raw = 4 * pre_c < x.nk ? fetch(pre_c) : kBeyond;
         return r;
@@ -953,17 +959,24 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
     bool ok = true;
     Item x;
     while (ok && next_item<kAlt, kFP8>(p, sm, idx, total, x, ncta)) {
+      // this warpgroup's fields of the item, in registers
+      const int nt = qt ? x.nt[1] : x.nt[0];
+      const int t0 = qt ? x.t0[1] : x.t0[0];
+      const int pos0 = qt ? x.pos0[1] : x.pos0[0];
+      const int first = qt ? x.first[1] : x.first[0];
+      const int last = qt ? x.last[1] : x.last[0];
+      const int step = x.step;
       const int tok = tid / g;  // token within the tile
       // rows past the tile's tokens compute on whatever Q holds there; their
       // output is never stored
-      const bool valid = tid < x.nt[qt] * g;
+      const bool valid = tid < nt * g;
       // shared-prefix mode: the warpgroup's partial slot of this key chunk
-      const size_t head = (size_t)(x.q0 + x.t0[qt] + tok) * p.num_heads + (size_t)x.kvh * g + tid % g;
+      const size_t head = (size_t)(x.q0 + t0 + tok) * p.num_heads + (size_t)x.kvh * g + tid % g;
       const int slot = 2 * x.chunk + qt;
-      if (x.last[qt] < 0) {
+      if (last < 0) {
         // no key tile for this warpgroup here (no tile b, or a one-tile chunk in
         // shared-prefix mode, whose empty partial then weighs nothing)
-        if (kAlt && valid && x.nt[qt] > 0 && slot < p.max_parts) {
+        if (kAlt && valid && nt > 0 && slot < p.max_parts) {
           p.lse[head * p.max_parts + slot] = -INFINITY;
           float4* z = reinterpret_cast<float4*>(p.o_part + (head * p.max_parts + slot) * kD);
 #pragma unroll 4
@@ -971,18 +984,17 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
         }
         continue;
       }
-      const int qpos = x.pos0[qt] + (kAlt ? 0 : tok);
+      const int qpos = pos0 + (kAlt ? 0 : tok);
       // E4M3 caches: the row's query scale s (q / s = hi + lo) joins the score scale
       const float qa_r = kFP8 ? qa * (valid ? __ldg(p.q8_scale + head) : 1.0f) : qa;
       // draft-tree mode: the row's visible chunk keys, from the chunk's first position
-      const int cbase = x.pos0[qt] - x.t0[qt];
-      const uint64_t tmask =
-          kTree && valid ? __ldg(p.tree_mask + x.q0 + x.t0[qt] + tok) : 0ull;
+      const int cbase = pos0 - t0;
+      const uint64_t tmask = kTree && valid ? __ldg(p.tree_mask + x.q0 + t0 + tok) : 0ull;
       float m_run = -INFINITY;
       float2 l2[4];  // partial row sums (independent chains, packed pairs)
 #pragma unroll
       for (int i = 0; i < 4; ++i) l2[i] = make_float2(0.0f, 0.0f);
-      for (int t = x.first[qt]; t <= x.last[qt]; t += x.step, ++ns) {
+      for (int t = first; t <= last; t += step, ++ns) {
         ok = all_group(wait_bar(&sm.s_ready[qt], ns & 1, abort, lim), qt);
         if (!ok) break;
         tc::fence_after_sync();
@@ -1019,7 +1031,7 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
             sv[c] = (vw[c >> 5] >> (c & 31)) & 1u ? sv[c] : -INFINITY;
             mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
           }
-        } else if (kbase + kTileKeys - 1 > x.pos0[qt]) {
+        } else if (kbase + kTileKeys - 1 > pos0) {
           // the causal boundary crosses this tile: hidden keys become -inf
 #pragma unroll
           for (int c = 0; c < kTileKeys; ++c) {
@@ -1039,7 +1051,7 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
         const bool need = mt > m_run + (kFP8 ? kRescaleAt8 : kRescaleAt);
         float alpha = 1.0f;
         if (need) {
-          alpha = (t == x.first[qt]) ? 0.0f : fast_exp2(m_run - mt);
+          alpha = (t == first) ? 0.0f : fast_exp2(m_run - mt);
           m_run = mt;
 #pragma unroll
           for (int i = 0; i < 4; ++i) l2[i] = __fmul2_rn(l2[i], make_float2(alpha, alpha));
@@ -1063,7 +1075,7 @@ __device__ __forceinline__ void prefill_body(const AttnParams& p, const CUtensor
           }
         }
         // the product of tile t adds onto O: rescale it first when a row's max moved
-        if (t > x.first[qt] && __any_sync(kFull, need)) {
+        if (t > first && __any_sync(kFull, need)) {
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             float ov[32];
