@@ -175,23 +175,54 @@ __device__ __forceinline__ int clamped_keys(const AttnParams& p, int s, bool rep
 // Items are the non-empty (sequence, partition) pairs in sequence order, each
 // split over the KV heads (KV head fastest): item k has KV head k % Hkv and
 // pair k / Hkv.  Consecutive items read neighbouring (block, head) tiles.
+//
+// A CTA visits items first, first + stride, ...  Its cursor carries the next
+// item's KV head and pair (advanced by adds, not divisions) and the sequence
+// of the last one: pairs only grow, so the next sequence is found by stepping
+// forward from there (a binary search for the first item, or when more than
+// a few sequences lie in between).  A trace of the 70B-GQA decode had the
+// divisions and the full binary search take ~1,250 SM cycles per item in
+// every warp role.
+struct Cursor {
+  int k, kvh, pair, seq;  // next item, its KV head and pair; sequence of the last (-1: none)
+  int dq, dr;             // stride = dq pairs + dr KV heads
+};
+
+__device__ __forceinline__ Cursor first_cursor(const AttnParams& p, int first, int stride) {
+  Cursor c;
+  c.k = first;
+  c.kvh = first % p.num_kv_heads;
+  c.pair = first / p.num_kv_heads;
+  c.seq = -1;
+  c.dq = stride / p.num_kv_heads;
+  c.dr = stride % p.num_kv_heads;
+  return c;
+}
+
 template <class SM>
-__device__ __forceinline__ bool next_item(const AttnParams& p, const SM& sm, int& idx,
+__device__ __forceinline__ bool next_item(const AttnParams& p, const SM& sm, Cursor& c,
                                           int total, Item& it, int stride) {
-  if (idx >= total) return false;
-  const int k = idx;
-  idx += stride;
-  const int kvh = k % p.num_kv_heads;
-  const int pair = k / p.num_kv_heads;
-  int lo = 0, hi = p.num_rows - 1;  // largest s with start(s) <= pair
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if ((sm.seq_pack[mid] >> kLenBits) <= pair) lo = mid; else hi = mid - 1;
+  if (c.k >= total) return false;
+  const int pair = c.pair;
+  const int S = p.num_rows;
+  // largest s with start(s) <= pair
+  int lo = c.seq < 0 ? 0 : c.seq, hi = S - 1;
+  int steps = c.seq < 0 ? 4 : 0;
+  while (steps < 4 && lo < hi && (sm.seq_pack[lo + 1] >> kLenBits) <= pair) {
+    ++lo;
+    ++steps;
   }
+  if (steps == 4) {
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((sm.seq_pack[mid] >> kLenBits) <= pair) lo = mid; else hi = mid - 1;
+    }
+  }
+  c.seq = lo;
   const int pk = sm.seq_pack[lo];
   const int start = pk >> kLenBits;
   it.seq = lo;
-  it.kvh = kvh;
+  it.kvh = c.kvh;
   it.part = pair - start;
   it.nparts = (sm.seq_pack[lo + 1] >> kLenBits) - start;
   it.n = it.part == it.nparts - 1 ? (pk & ((1 << kLenBits) - 1)) + 1 : kPart;
@@ -201,6 +232,13 @@ __device__ __forceinline__ bool next_item(const AttnParams& p, const SM& sm, int
   if (p.prefix_lens != nullptr) {  // cascade decode: the keys after the shared prefix
     it.kstart = cascade_prefix(p, lo, clamped_keys(p, lo, false), false);
     it.slot += cascade_slots(p, it.kstart);
+  }
+  c.k += stride;
+  c.pair += c.dq;
+  c.kvh += c.dr;
+  if (c.kvh >= p.num_kv_heads) {
+    c.kvh -= p.num_kv_heads;
+    ++c.pair;
   }
   return true;
 }
@@ -453,7 +491,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
     uint64_t* empty = is_v ? sm.vempty : sm.kempty;
     const uint32_t nst = is_v ? VS : KS;
     uint8_t* ring = is_v ? &sm.vring[0][0] : &sm.kring[0][0];
-    int idx = cta;
+    Cursor idx = first_cursor(p, cta, ncta);
     uint32_t pos = 0;
     int it = 0;
     bool ok = true;
@@ -542,7 +580,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
       auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
         return __shfl_sync(kFull, (int)wait_bar(bar, parity, abort, lim), 0) != 0;
       };
-      int idx = cta;
+      Cursor idx = first_cursor(p, cta, ncta);
       uint32_t kpos = 0, vpos = 0;
       int ntail = 0;  // items with a partial last block so far
       Item cur;
@@ -676,7 +714,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
     // ---- tail loader (16-bit: warp 7) / query converters + tail loader (E4M3: 7-10) -----
     constexpr int kGroup = FP8 ? 128 : 32;
     const int gtid = threadIdx.x - 224;
-    int idx = cta;
+    Cursor idx = first_cursor(p, cta, ncta);
     int it = 0, ntail = 0;
     bool ok = true;
     auto group_all = [&](bool v) -> bool {
@@ -854,7 +892,7 @@ __device__ __forceinline__ void decode_body(const AttnParams& p, const CUtensorM
         }
       }
     }
-    int idx = cta;
+    Cursor idx = first_cursor(p, cta, ncta);
     Item cur, nxt, prev;
     int it = 0;
     bool has = next_item(p, sm, idx, total, cur, ncta);
