@@ -13,10 +13,11 @@
 //   (shuffle reductions for the max and the sum); each lane owns four output
 //   dimensions (one float4 of each partial) and walks the partitions with
 //   four loads in flight, taking each weight from its lane by shuffle;
-// - many partitions: one CTA of eight warps per (row, head).  The weights go
-//   to shared memory once; warp w takes partitions w, w + 8, ... for all
-//   dimensions (float4 per lane) and the eight partial sums meet in shared
-//   memory.
+// - many partitions: one CTA of sixteen warps per (row, head).  The weights
+//   go to shared memory once; warp w takes partitions w, w + 16, ... for all
+//   dimensions (float4 per lane), its first eight partials requested before
+//   the weights and eight in flight after, and the sixteen partial sums meet
+//   in shared memory.
 // Either way every partial is read once, with 16-byte loads.
 
 #include "common.cuh"
@@ -53,6 +54,14 @@ __device__ __forceinline__ void store4(OutT* dst, float4 v) {
   store_out(dst + 3, v.w);
 }
 
+// The merge is launched as a programmatic dependent of the attention launch
+// before it (its launch overlaps that grid's end); it reads the partials only
+// once that grid has completed and its writes are visible.  Without the
+// launch attribute this returns at once.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ float4 fma4(float w, const float4& a, float4 c) {
   c.x = fmaf(w, a.x, c.x);
   c.y = fmaf(w, a.y, c.y);
@@ -65,6 +74,7 @@ __device__ __forceinline__ float4 fma4(float w, const float4& a, float4 c) {
 template <class QT, int D>
 __global__ void __launch_bounds__(32 * kMergeWarps) lse_merge_warp_kernel(const AttnParams p) {
   using OutT = typename QT::T;
+  grid_dependency_wait();
   const int lane = threadIdx.x & 31;
   const long long pair = (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   if (pair >= (long long)p.num_rows * p.num_heads) return;
@@ -124,12 +134,15 @@ __global__ void __launch_bounds__(32 * kMergeWarps) lse_merge_warp_kernel(const 
                                      ((a0.w + a1.w) + (a2.w + a3.w)) * inv));
 }
 
-// One CTA of eight warps per (row, head), for many partitions.
+// One CTA of sixteen warps per (row, head), for many partitions.
+constexpr int kCtaWarps = 16;
+
 template <class QT, int D>
-__global__ void __launch_bounds__(32 * kMergeWarps) lse_merge_cta_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(32 * kCtaWarps) lse_merge_cta_kernel(const AttnParams p) {
   using OutT = typename QT::T;
-  extern __shared__ float s_w[];  // [max_parts] weights, then [kMergeWarps][D] partial sums
-  __shared__ float s_red[kMergeWarps];
+  extern __shared__ float s_w[];  // [max_parts] weights, then [kCtaWarps][D] partial sums
+  __shared__ float s_red[kCtaWarps];
+  grid_dependency_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x, h = blockIdx.y;
   const int np = row_parts(p, row);
@@ -141,19 +154,33 @@ __global__ void __launch_bounds__(32 * kMergeWarps) lse_merge_cta_kernel(const A
     if (tid < kLanes) store4(out + 4 * tid, make_float4(0.f, 0.f, 0.f, 0.f));
     return;
   }
+  // warp w's partitions are w, w + W, ...: its first kIn partials are
+  // requested before the weights are known (their latency overlaps the
+  // log-sum-exp pass), then kIn stay in flight
+  constexpr int W = kCtaWarps;
+  constexpr int kIn = 8;
+  constexpr int kStride = D / 4;
+  const float4* op = reinterpret_cast<const float4*>(p.o_part + head * p.max_parts * D) + lane;
+  const bool dims = lane < kLanes;
+  float4 pf[kIn];
+#pragma unroll
+  for (int j = 0; j < kIn; ++j) {
+    const int i = warp + j * W;
+    pf[j] = dims && i < np ? __ldg(op + (size_t)i * kStride) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   const float* lse = p.lse + head * p.max_parts;
   float m = -INFINITY;
-  for (int i = tid; i < np; i += 32 * kMergeWarps) m = fmaxf(m, __ldg(lse + i));
+  for (int i = tid; i < np; i += 32 * W) m = fmaxf(m, __ldg(lse + i));
 #pragma unroll
   for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
   if (lane == 0) s_red[warp] = m;
   __syncthreads();
   m = s_red[0];
 #pragma unroll
-  for (int w = 1; w < kMergeWarps; ++w) m = fmaxf(m, s_red[w]);
+  for (int w = 1; w < W; ++w) m = fmaxf(m, s_red[w]);
   __syncthreads();
   float sum = 0.0f;
-  for (int i = tid; i < np; i += 32 * kMergeWarps) {
+  for (int i = tid; i < np; i += 32 * W) {
     const float e = exp2f(__ldg(lse + i) - m);
     s_w[i] = e;
     sum += e;
@@ -164,56 +191,75 @@ __global__ void __launch_bounds__(32 * kMergeWarps) lse_merge_cta_kernel(const A
   __syncthreads();
   sum = 0.0f;
 #pragma unroll
-  for (int w = 0; w < kMergeWarps; ++w) sum += s_red[w];
+  for (int w = 0; w < W; ++w) sum += s_red[w];
   float* s_acc = s_w + ((p.max_parts + 3) & ~3);
-  if (lane < kLanes) {
-    const float4* op =
-        reinterpret_cast<const float4*>(p.o_part + head * p.max_parts * D) + lane;
-    constexpr int kStride = D / 4;
-    constexpr int W = kMergeWarps;
-    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
-    int i = warp;
-    for (; i + 3 * W < np; i += 4 * W) {  // four loads in flight
-      const float4 v0 = __ldg(op + (size_t)i * kStride);
-      const float4 v1 = __ldg(op + (size_t)(i + W) * kStride);
-      const float4 v2 = __ldg(op + (size_t)(i + 2 * W) * kStride);
-      const float4 v3 = __ldg(op + (size_t)(i + 3 * W) * kStride);
-      a0 = fma4(s_w[i], v0, a0);
-      a1 = fma4(s_w[i + W], v1, a1);
-      a2 = fma4(s_w[i + 2 * W], v2, a2);
-      a3 = fma4(s_w[i + 3 * W], v3, a3);
+  float4 a[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) a[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int base = 0;; base += kIn) {
+    // partials base .. base + kIn - 1 of this warp are in pf
+#pragma unroll
+    for (int j = 0; j < kIn; ++j) {
+      const int i = warp + (base + j) * W;
+      if (i < np) a[j & 3] = fma4(s_w[i], pf[j], a[j & 3]);
     }
-    for (; i < np; i += W) a0 = fma4(s_w[i], __ldg(op + (size_t)i * kStride), a0);
-    reinterpret_cast<float4*>(s_acc + warp * D)[lane] =
-        make_float4((a0.x + a1.x) + (a2.x + a3.x), (a0.y + a1.y) + (a2.y + a3.y),
-                    (a0.z + a1.z) + (a2.z + a3.z), (a0.w + a1.w) + (a2.w + a3.w));
+    if (warp + (base + kIn) * W >= np) break;
+#pragma unroll
+    for (int j = 0; j < kIn; ++j) {
+      const int i = warp + (base + kIn + j) * W;
+      pf[j] = dims && i < np ? __ldg(op + (size_t)i * kStride) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
+  if (dims)
+    reinterpret_cast<float4*>(s_acc + warp * D)[lane] =
+        make_float4((a[0].x + a[1].x) + (a[2].x + a[3].x), (a[0].y + a[1].y) + (a[2].y + a[3].y),
+                    (a[0].z + a[1].z) + (a[2].z + a[3].z), (a[0].w + a[1].w) + (a[2].w + a[3].w));
   __syncthreads();
   if (tid < D) {
     float acc = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) acc += s_acc[w * D + tid];
+    for (int w = 0; w < W; ++w) acc += s_acc[w * D + tid];
     store_out(out + tid, acc / sum);
   }
 }
 
+// Launches kernel k on `stream` as a programmatic dependent of the launch
+// before it (the kernels wait for it with grid_dependency_wait).
+template <class K>
+int launch_dependent(K k, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                     const AttnParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, p) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 template <class QT, int D>
 int launch_merge_shape(const AttnParams& p, cudaStream_t stream) {
+  int rc;
   if (p.max_parts <= kWarpParts) {
     const long long pairs = (long long)p.num_rows * p.num_heads;
     const long long ctas = (pairs + kMergeWarps - 1) / kMergeWarps;
     if (ctas > 0x7fffffff) return PKV_ERR_UNSUPPORTED;
-    lse_merge_warp_kernel<QT, D><<<(unsigned)ctas, 32 * kMergeWarps, 0, stream>>>(p);
+    rc = launch_dependent(lse_merge_warp_kernel<QT, D>, dim3((unsigned)ctas),
+                          dim3(32 * kMergeWarps), 0, stream, p);
   } else {
     auto k = lse_merge_cta_kernel<QT, D>;
-    const size_t smem = ((size_t)(p.max_parts + 3) / 4 * 4 + kMergeWarps * D) * sizeof(float);
+    const size_t smem = ((size_t)(p.max_parts + 3) / 4 * 4 + kCtaWarps * D) * sizeof(float);
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
       return PKV_ERR_CUDA;
-    k<<<dim3(p.num_rows, p.num_heads), 32 * kMergeWarps, smem, stream>>>(p);
+    rc = launch_dependent(k, dim3(p.num_rows, p.num_heads), dim3(32 * kCtaWarps), smem, stream, p);
   }
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return rc == PKV_OK && cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 template <class QT>
