@@ -515,7 +515,9 @@ int pkv_paged_attention_decode_cascade(void* out, const void* q, const void* k_c
     rc = pkv::launch_prefill_tc(pp, q_dtype, num_seqs, st);
     if (rc != PKV_OK) return rc;
   }
-  rc = pkv::launch_paged_decode_tc(ps, q_dtype, kv_dtype, st);
+  // the own-keys pass reads nothing the prefix pass writes: it may fill the
+  // prefix pass's last wave (programmatic dependent launch)
+  rc = pkv::launch_paged_decode_tc(ps, q_dtype, kv_dtype, st, num_groups > 0 && max_prefix_len > 0);
   if (rc != PKV_OK) return rc;
   return pkv::launch_lse_merge(ps, q_dtype, head_dim, st);
 }

@@ -15,13 +15,17 @@ __global__ void __launch_bounds__(tc_threads(G16, FP8), 1)
                            const __grid_constant__ CUtensorMap tm_v,
                            const __grid_constant__ CUtensorMap tm_q, int kv_rows) {
   extern __shared__ uint8_t smem_raw[];
+  // launched as a dependent (cascade decode), this grid does not read its
+  // predecessor but ends only after it.  (Letting the merge start early here
+  // was measured slower: its resident CTAs slowed the decode.)
   decode_body<QT, G16, FP8, tc_threads(G16, FP8), kH>(p, tm_k, tm_v, tm_q, kv_rows, blockIdx.x,
                                                      gridDim.x, smem_raw);
+  tc::grid_dependency_wait();
 }
 
 // ---- host side ---------------------------------------------------------------------------
 template <class QT, bool G16, bool FP8, int kH = (G16 ? 16 : 8)>
-int launch_tc_typed(const AttnParams& p, cudaStream_t stream) {
+int launch_tc_typed(const AttnParams& p, cudaStream_t stream, bool dependent) {
   const bool bf16 = std::is_same<QT, BF16>::value;
   const uint64_t kv_rows = (uint64_t)p.num_blocks * p.num_kv_heads * kBlockSize;
   CUtensorMap tk, tv;
@@ -71,7 +75,22 @@ int launch_tc_typed(const AttnParams& p, cudaStream_t stream) {
     int grid = sm_count();
     if (items < grid) grid = (int)items;
     if (grid < 1) grid = 1;
-    kern<<<grid, tc_threads(G16, FP8), smem, stream>>>(c, tk, tv, tq, (int)kv_rows);
+    if (dependent && r0 == 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(grid);
+      cfg.blockDim = dim3(tc_threads(G16, FP8));
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr.val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      if (cudaLaunchKernelEx(&cfg, kern, c, tk, tv, tq, (int)kv_rows) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    } else {
+      kern<<<grid, tc_threads(G16, FP8), smem, stream>>>(c, tk, tv, tq, (int)kv_rows);
+    }
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   }
   return PKV_OK;
@@ -92,24 +111,25 @@ bool tc_decode_supported(const AttnParams& p, int q_dtype, int kv_dtype, int hea
   return tmap_available();
 }
 
-int launch_paged_decode_tc(const AttnParams& p, int q_dtype, int kv_dtype, cudaStream_t stream) {
+int launch_paged_decode_tc(const AttnParams& p, int q_dtype, int kv_dtype, cudaStream_t stream,
+                           bool dependent) {
   const bool g16 = p.group > 8, g4 = p.group <= 4;
   if (kv_dtype == PKV_FP8_E4M3) {
     if (q_dtype == PKV_BF16)
-      return g16  ? launch_tc_typed<BF16, true, true>(p, stream)
-             : g4 ? launch_tc_typed<BF16, false, true, 4>(p, stream)
-                  : launch_tc_typed<BF16, false, true>(p, stream);
-    return g16  ? launch_tc_typed<F16, true, true>(p, stream)
-           : g4 ? launch_tc_typed<F16, false, true, 4>(p, stream)
-                : launch_tc_typed<F16, false, true>(p, stream);
+      return g16  ? launch_tc_typed<BF16, true, true>(p, stream, dependent)
+             : g4 ? launch_tc_typed<BF16, false, true, 4>(p, stream, dependent)
+                  : launch_tc_typed<BF16, false, true>(p, stream, dependent);
+    return g16  ? launch_tc_typed<F16, true, true>(p, stream, dependent)
+           : g4 ? launch_tc_typed<F16, false, true, 4>(p, stream, dependent)
+                : launch_tc_typed<F16, false, true>(p, stream, dependent);
   }
   if (q_dtype == PKV_BF16)
-    return g16  ? launch_tc_typed<BF16, true, false>(p, stream)
-           : g4 ? launch_tc_typed<BF16, false, false, 4>(p, stream)
-                : launch_tc_typed<BF16, false, false>(p, stream);
-  return g16  ? launch_tc_typed<F16, true, false>(p, stream)
-         : g4 ? launch_tc_typed<F16, false, false, 4>(p, stream)
-              : launch_tc_typed<F16, false, false>(p, stream);
+    return g16  ? launch_tc_typed<BF16, true, false>(p, stream, dependent)
+           : g4 ? launch_tc_typed<BF16, false, false, 4>(p, stream, dependent)
+                : launch_tc_typed<BF16, false, false>(p, stream, dependent);
+  return g16  ? launch_tc_typed<F16, true, false>(p, stream, dependent)
+         : g4 ? launch_tc_typed<F16, false, false, 4>(p, stream, dependent)
+              : launch_tc_typed<F16, false, false>(p, stream, dependent);
 }
 
 }  // namespace pkv

@@ -91,7 +91,12 @@ int launch_simt_bf16_e4m3(const AttnParams& p, int head_dim, int g_pad, cudaStre
 // tcgen05 grouped-query decode (head_dim 128, 16-bit or E4M3 caches, 2..16
 // heads per KV head, 512-token partitions, decode rows only).
 bool tc_decode_supported(const AttnParams& p, int q_dtype, int kv_dtype, int head_dim);
-int launch_paged_decode_tc(const AttnParams& p, int q_dtype, int kv_dtype, cudaStream_t stream);
+// dependent: launched as a programmatic dependent of the launch before it on
+// the stream, which it does not read; its CTAs may start while that grid ends
+// and wait for it before they exit (so whatever waits for this grid also
+// sees that one's writes).
+int launch_paged_decode_tc(const AttnParams& p, int q_dtype, int kv_dtype, cudaStream_t stream,
+                           bool dependent = false);
 
 // tcgen05 chunked-prefill attention (head_dim 128, 16-bit caches, 128 % g == 0).
 bool tc_prefill_supported(const AttnParams& p, int q_dtype, int kv_dtype, int head_dim);

@@ -27,6 +27,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_q, int kv_rows) {
   extern __shared__ uint8_t smem_raw[];
+  // shared-prefix pass: the cascade's own-keys decode, launched after it as a
+  // dependent, may start on the SMs this grid's last wave leaves free
+  if constexpr (kAlt) tc::launch_dependents();
   prefill_body<QT, kTree, kAlt, kFP8>(p, tm_k, tm_v, tm_q, kv_rows, blockIdx.x, gridDim.x,
                                       smem_raw);
 }

@@ -197,6 +197,18 @@ __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// ---- programmatic dependent launch ----------------------------------------------------
+// Lets a kernel launched after this one with the programmatic-serialization
+// attribute start (it must wait for this grid before reading its results).
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the grid this one was launched as a dependent of has completed
+// and its writes are visible (returns at once for an ordinary launch).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- CTA pairs (cta_group::2) --------------------------------------------------------
 // Two CTAs of a cluster share one MMA tile of M = 256 rows: each holds 128
 // rows of A (smem or TMEM) and half of the N columns of B, both at the same
