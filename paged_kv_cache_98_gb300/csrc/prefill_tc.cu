@@ -36,47 +36,57 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // The query of an E4M3-cache prefill, split per (row, head) for 8-bit MMAs:
 // q / s = hi + lo with hi = E4M3(q / s), lo = E4M3(q / s - hi) and
-// s = max|q| / 448 (1 for a zero row); together about 8 significant bits.  A
-// warp per (row, head), four elements per lane.  hi rows [rows][heads][128 B],
-// then the lo rows, then s [rows][heads].
+// s = max|q| / 448 (1 for a zero row); together about 8 significant bits.
+// Sixteen lanes per (row, head), eight elements (one 16-byte load) per lane;
+// each half-warp splits kPerHalf consecutive (row, head)s, their loads issued
+// first.  hi rows [rows][heads][128 B], then the lo rows, then s [rows][heads].
+constexpr int kPerHalf = 2;
+
 template <class QT>
 __global__ void __launch_bounds__(256) split_query_kernel(const typename QT::T* __restrict__ q,
                                                           uint8_t* __restrict__ hi,
                                                           uint8_t* __restrict__ lo,
                                                           float* __restrict__ scale,
                                                           long long row_heads) {
-  const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (w >= row_heads) return;  // (whole warps)
-  const uint2 raw = __ldg(reinterpret_cast<const uint2*>(q + w * kD) + lane);
-  float f[4];
-  {
-    uint4 wide = make_uint4(raw.x, raw.y, 0, 0);
-    float f8[8];
-    to_float(wide, f8, QT());
+  const long long half = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 4;
+  const int lane = threadIdx.x & 15;
+  uint4 raw[kPerHalf];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) f[i] = f8[i];
+  for (int j = 0; j < kPerHalf; ++j) {
+    const long long w = half * kPerHalf + j;
+    raw[j] = w < row_heads ? __ldg(reinterpret_cast<const uint4*>(q + w * kD) + lane)
+                           : make_uint4(0, 0, 0, 0);
   }
-  float amax = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
 #pragma unroll
-  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-  const float inv = amax > 0.0f ? 448.0f / amax : 1.0f;
-  uint32_t h4 = 0, l4 = 0;
+  for (int j = 0; j < kPerHalf; ++j) {
+    const long long w = half * kPerHalf + j;
+    float f[8];
+    to_float(raw[j], f, QT());
+    float amax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 4; i += 2) {
-    const float x0 = f[i] * inv, x1 = f[i + 1] * inv;
-    const __nv_fp8x2_storage_t h2 =
-        __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
-    __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3);
-    const float2 hv = __half22float2(*reinterpret_cast<__half2*>(&hr));
-    const __nv_fp8x2_storage_t l2 =
-        __nv_cvt_float2_to_fp8x2(make_float2(x0 - hv.x, x1 - hv.y), __NV_SATFINITE, __NV_E4M3);
-    h4 |= (uint32_t)h2 << (8 * i);
-    l4 |= (uint32_t)l2 << (8 * i);
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+    for (int o = 8; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o, 16));
+    const float inv = amax > 0.0f ? 448.0f / amax : 1.0f;
+    uint32_t h4[2] = {0, 0}, l4[2] = {0, 0};
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      const float x0 = f[i] * inv, x1 = f[i + 1] * inv;
+      const __nv_fp8x2_storage_t h2 =
+          __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+      __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3);
+      const float2 hv = __half22float2(*reinterpret_cast<__half2*>(&hr));
+      const __nv_fp8x2_storage_t l2 =
+          __nv_cvt_float2_to_fp8x2(make_float2(x0 - hv.x, x1 - hv.y), __NV_SATFINITE, __NV_E4M3);
+      h4[i >> 2] |= (uint32_t)h2 << (8 * (i & 3));
+      l4[i >> 2] |= (uint32_t)l2 << (8 * (i & 3));
+    }
+    if (w < row_heads) {
+      reinterpret_cast<uint2*>(hi + w * kD)[lane] = make_uint2(h4[0], h4[1]);
+      reinterpret_cast<uint2*>(lo + w * kD)[lane] = make_uint2(l4[0], l4[1]);
+      if (lane == 0) scale[w] = amax > 0.0f ? amax / 448.0f : 1.0f;
+    }
   }
-  reinterpret_cast<uint32_t*>(hi + w * kD)[lane] = h4;
-  reinterpret_cast<uint32_t*>(lo + w * kD)[lane] = l4;
-  if (lane == 0) scale[w] = amax > 0.0f ? amax / 448.0f : 1.0f;
 }
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
@@ -221,7 +231,8 @@ int launch_prefill_tc_fp8(const AttnParams& p, int q_dtype, int total_q, void* w
   uint8_t* hi = static_cast<uint8_t*>(workspace);
   uint8_t* lo = hi + rh * kD;
   float* scale = reinterpret_cast<float*>(hi + round256(2 * rh * kD));
-  const long long blocks = ((long long)rh * 32 + 255) / 256;
+  // sixteen threads per kPerHalf (row, head)s
+  const long long blocks = (((long long)rh + kPerHalf - 1) / kPerHalf * 16 + 255) / 256;
   if (blocks > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
   AttnParams c = p;
   c.q8_scale = scale;
